@@ -1,0 +1,158 @@
+"""fp64 CPU oracle of the ReDrafter verification step -- TEST INFRASTRUCTURE.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg
+may import this package.  It shares no code with the CUDA library and never
+imports it.  The arithmetic lives in ``rd_oracle.c`` (plain C, fp64); this
+module compiles it with gcc, marshals numpy arrays into it, and adds
+``oracle_unpack``, the gather written as plain numpy indexing.
+
+Each function states the passage it follows in the C source; the unpack gather
+follows the PyTorch listing in the NVIDIA blog "ReDrafter in TensorRT-LLM",
+section "Implementing in-Engine Validation and Drafting" (gather along the
+packed dimension with the unpacker as index, reshaped to [B, W, L, D]).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import sys
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "rd_oracle.c")
+_LIB = os.path.join(_HERE, "librd_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile rd_oracle.c into librd_oracle.so (gcc, -O2, no fast-math)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm",
+               "-lpthread"]
+        subprocess.check_call(cmd)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            lib.oracle_pack.argtypes = [P, I, I, I, I, P, P, P, P, P, P]
+            lib.oracle_tree_attention.argtypes = [I, I, I, I, I, ctypes.c_double, P, P, P, P,
+                                                  P, P, P, P, I, P, I]
+            lib.oracle_causal_attention.argtypes = [I, I, I, I, ctypes.c_double, P, P, P, P,
+                                                    P, I]
+            lib.oracle_greedy_accept.argtypes = [P, I, I, I, P, P, P, I, I, P, P, P, P, P]
+            for f in (lib.oracle_pack, lib.oracle_tree_attention,
+                      lib.oracle_causal_attention, lib.oracle_greedy_accept):
+                f.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def n_threads_default() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def oracle_pack(beams: np.ndarray, P_cap: int | None = None) -> dict:
+    """Prefix dedup of [B, W, L] beams (see oracle_pack in rd_oracle.c)."""
+    beams = _c(beams, np.int32)
+    B, W, L = beams.shape
+    P_cap = W * L if P_cap is None else P_cap
+    NW = (P_cap + 31) // 32
+    out = dict(tokens=np.zeros((B, P_cap), np.int32), packer=np.zeros((B, P_cap), np.int32),
+               unpacker=np.zeros((B, W, L), np.int32),
+               mask=np.zeros((B, P_cap, NW), np.uint32), depth=np.zeros((B, P_cap), np.int32),
+               packed_len=np.zeros(B, np.int32))
+    rc = _load().oracle_pack(_ptr(beams), B, W, L, P_cap, _ptr(out["tokens"]),
+                             _ptr(out["packer"]), _ptr(out["unpacker"]), _ptr(out["mask"]),
+                             _ptr(out["depth"]), _ptr(out["packed_len"]))
+    if rc != 0:
+        raise ValueError(f"oracle_pack rejected the input (rc={rc})")
+    return out
+
+
+def oracle_tree_attention(q, k_new, v_new, k_cache, v_cache, ctx_offsets, packed_len,
+                          mask, scale: float = 0.0, n_threads: int | None = None
+                          ) -> np.ndarray:
+    """Tree-masked attention in fp64.  bf16 inputs as uint16 bit arrays:
+    q [B,P,Hq,D], k_new/v_new [B,P,Hkv,D], k_cache/v_cache [sum C, Hkv, D],
+    ctx_offsets int64 [B+1], packed_len int32 [B], mask uint32 [B,P,NW].
+    Returns float64 [B,P,Hq,D]."""
+    q = _c(q, np.uint16); k_new = _c(k_new, np.uint16); v_new = _c(v_new, np.uint16)
+    k_cache = _c(k_cache, np.uint16); v_cache = _c(v_cache, np.uint16)
+    ctx_offsets = _c(ctx_offsets, np.int64); packed_len = _c(packed_len, np.int32)
+    mask = _c(mask, np.uint32)
+    B, P, Hq, D = q.shape
+    Hkv = k_new.shape[2]
+    o = np.zeros((B, P, Hq, D), np.float64)
+    rc = _load().oracle_tree_attention(B, P, Hq, Hkv, D, float(scale), _ptr(q), _ptr(k_new),
+                                       _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                       _ptr(ctx_offsets), _ptr(packed_len), _ptr(mask),
+                                       mask.shape[2], _ptr(o),
+                                       n_threads or n_threads_default())
+    if rc != 0:
+        raise ValueError(f"oracle_tree_attention rejected the input (rc={rc})")
+    return o
+
+
+def oracle_causal_attention(q, k, v, cu_seqlens, scale: float = 0.0,
+                            n_threads: int | None = None) -> np.ndarray:
+    """Causal attention per sequence in fp64: q [T,Hq,D], k/v [T,Hkv,D] (uint16 bf16 bits),
+    cu_seqlens int32 [Bc+1].  Returns float64 [T,Hq,D]."""
+    q = _c(q, np.uint16); k = _c(k, np.uint16); v = _c(v, np.uint16)
+    cu = _c(cu_seqlens, np.int32)
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    o = np.zeros((T, Hq, D), np.float64)
+    rc = _load().oracle_causal_attention(len(cu) - 1, Hq, Hkv, D, float(scale), _ptr(q),
+                                         _ptr(k), _ptr(v), _ptr(cu), _ptr(o),
+                                         n_threads or n_threads_default())
+    if rc != 0:
+        raise ValueError(f"oracle_causal_attention rejected the input (rc={rc})")
+    return o
+
+
+def oracle_greedy_accept(logits, beams, unpacker, packed_len) -> dict:
+    """Greedy verification: logits [B,P,V] (uint16 bf16 bits), beams/unpacker [B,W,L]."""
+    logits = _c(logits, np.uint16); beams = _c(beams, np.int32)
+    unpacker = _c(unpacker, np.int32); packed_len = _c(packed_len, np.int32)
+    B, P, V = logits.shape
+    W, L = beams.shape[1], beams.shape[2]
+    out = dict(argmax=np.zeros((B, P), np.int32), accept_len=np.zeros((B, W), np.int32),
+               best_beam=np.zeros(B, np.int32), n_accepted=np.zeros(B, np.int32),
+               out_tokens=np.zeros((B, L), np.int32))
+    rc = _load().oracle_greedy_accept(_ptr(logits), B, P, V, _ptr(beams), _ptr(unpacker),
+                                      _ptr(packed_len), W, L, _ptr(out["argmax"]),
+                                      _ptr(out["accept_len"]), _ptr(out["best_beam"]),
+                                      _ptr(out["n_accepted"]), _ptr(out["out_tokens"]))
+    if rc != 0:
+        raise ValueError(f"oracle_greedy_accept rejected the input (rc={rc})")
+    return out
+
+
+def oracle_unpack(packed: np.ndarray, unpacker: np.ndarray) -> np.ndarray:
+    """out[b, w, i, :] = packed[b, unpacker[b, w, i], :] (any dtype, exact copy)."""
+    B, W, L = unpacker.shape
+    assert packed.ndim == 3 and packed.shape[0] == B
+    bidx = np.arange(B)[:, None, None]
+    return packed[bidx, unpacker]
