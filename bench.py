@@ -1,0 +1,401 @@
+#!/usr/bin/env python
+"""Benchmark of the ReDrafter verification step on GB300.
+
+One step = rd_pack_beams + rd_tree_attention + rd_greedy_accept + rd_unpack over
+one batch of the 13B-shaped workload (B=64 requests, W=8 beams x L=6 tokens,
+40/40 heads x 128, context 8192, vocab 32000, hidden 5120), seeded synthetic
+inputs resident in HBM.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (test infrastructure) on the host
+cores on a bounded sample of the same workload, scaled to the same metric.
+For N > 1 (torchrun, one rank per GPU) every rank verifies its own batch
+(weak scaling, no collective on the data path); the step time is the maximum
+over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "verify_steps_per_s"
+UNIT = "steps/s"
+FALLBACK_HBM_GBS = 6800.0
+ATTN_SRC = os.path.join(ROOT, "tree_attention_verify_gb300", "csrc", "attention_mma.cu")
+
+
+# ----------------------------------------------------------------------------
+# helpers
+# ----------------------------------------------------------------------------
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="13b_b64", choices=list(workloads.CONFIGS))
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-sample-requests", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's request count (small profiling runs)")
+    return ap.parse_args()
+
+
+def _config(args):
+    import dataclasses
+    cfg = workloads.CONFIGS[args.workload]
+    if args.batch > 0:
+        cfg = dataclasses.replace(cfg, B=args.batch, name=f"{cfg.name}_B{args.batch}")
+    return cfg
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _sha256(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def _profile_traffic(workload: str):
+    """DRAM bytes per launch of the attention kernel from the committed ncu summary,
+    or None if there is none or the kernel source changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"tree_attention_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m1 = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m2 = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
+    if not m1 or not m2 or m2.group(1) != _sha256(ATTN_SRC):
+        return None
+    return float(m1.group(1))
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        rows = [r.split(", ") for r in open(self.file.name).read().strip().splitlines()]
+        os.unlink(self.file.name)
+        mhz, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 10:
+                continue
+            try:
+                mhz.append(float(r[2]))
+                mx.append(float(r[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[6:10]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        if not mhz:
+            return None
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+def attention_bytes(cfg, ctx_lens, packed_len) -> float:
+    """Algorithmic HBM bytes of one rd_tree_attention launch: per (request, kv head)
+    4*D*(C_b + P_b) bytes of K/V (context and drafts) plus 4*G*D*P_b bytes of q and o,
+    plus the mask rows, offsets and lengths."""
+    G = cfg.Hq // cfg.Hkv
+    NW = (cfg.P_max + 31) // 32
+    C = np.asarray(ctx_lens, np.float64)
+    P = np.asarray(packed_len, np.float64)
+    per_b = cfg.Hkv * (4.0 * cfg.D * (C + P) + 4.0 * G * cfg.D * P) + 4.0 * NW * P
+    return float(per_b.sum() + cfg.B * 12 + 8)
+
+
+# ----------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline / reference arm)
+# ----------------------------------------------------------------------------
+def oracle_sample_time(inp, n_req: int, n_heads=None):
+    """Time the oracle on the first n_req requests (all kv heads unless n_heads is
+    given, then only the first n_heads kv heads of request 0).  Returns
+    (seconds, fraction of a full step that the sample covers, threads)."""
+    import oracle
+    bits = workloads.bf16_bits
+    cfg = inp["cfg"]
+    G = cfg.Hq // cfg.Hkv
+    offs = inp["ctx_offsets"].cpu().numpy()
+    n_req = max(1, min(n_req, cfg.B))
+    beams = inp["beams"][:n_req].cpu().numpy()
+    hs = cfg.Hkv if n_heads is None else max(1, min(n_heads, cfg.Hkv))
+    sub = dict(q=bits(inp["q"][:n_req, :, : hs * G]), kd=bits(inp["k_draft"][:n_req, :, :hs]),
+               vd=bits(inp["v_draft"][:n_req, :, :hs]),
+               kc=bits(inp["k_cache"][: int(offs[n_req]), :hs]),
+               vc=bits(inp["v_cache"][: int(offs[n_req]), :hs]),
+               logits=bits(inp["logits"][:n_req]), hidden=bits(inp["hidden"][:n_req]))
+    threads = oracle.n_threads_default()
+    oracle.build()
+    t0 = time.perf_counter()
+    pk = oracle.oracle_pack(beams, cfg.P_max)
+    oracle.oracle_tree_attention(sub["q"], sub["kd"], sub["vd"], sub["kc"], sub["vc"],
+                                 offs[: n_req + 1], pk["packed_len"], pk["mask"],
+                                 n_threads=threads)
+    oracle.oracle_greedy_accept(sub["logits"], beams, pk["unpacker"], pk["packed_len"])
+    oracle.oracle_unpack(sub["hidden"], pk["unpacker"])
+    dt = time.perf_counter() - t0
+    frac = (n_req / cfg.B) * (hs / cfg.Hkv)
+    return dt, frac, threads
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    cfg = _config(args)
+    inp = workloads.make_verify_inputs(cfg, device="cuda" if torch.cuda.is_available() else "cpu")
+    # size each step so that warmup + steps end within about two minutes
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    probe_dt, probe_frac, threads = oracle_sample_time(inp, 1, n_heads=1)
+    n_heads = max(1, min(cfg.Hkv, int(budget / max(probe_dt, 1e-3))))
+    for _ in range(args.warmup):
+        oracle_sample_time(inp, 1, n_heads=n_heads)
+    times, frac = [], None
+    for _ in range(args.steps):
+        dt, frac, threads = oracle_sample_time(inp, 1, n_heads=n_heads)
+        times.append(dt / frac)                 # seconds per full step
+    step_s = statistics.mean(times)
+    value = 1.0 / step_s
+    sample = (f"per step: request 0, {n_heads} of {cfg.Hkv} kv heads of tree attention plus its "
+              f"pack/accept/unpack, scaled by {1 / frac:.0f}x to a full {cfg.B}-request step")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": cfg.name, "B": cfg.B, "W": cfg.W, "L": cfg.L, "Hq": cfg.Hq,
+                       "Hkv": cfg.Hkv, "D": cfg.D, "context": cfg.ctx[1], "vocab": cfg.vocab,
+                       "Dh": cfg.Dh},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# our CUDA path
+# ----------------------------------------------------------------------------
+def run_ours(args):
+    import tree_attention_verify_gb300 as rd
+    from tree_attention_verify_gb300.step import VerifyStep
+
+    world, rank, local = _dist()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        pg = dist
+
+    cfg = _config(args)
+    inp = workloads.make_verify_inputs(cfg, device=dev, seed=cfg.seed + 1000 * rank)
+    max_ctx = int(inp["ctx_lens"].max())
+    step = VerifyStep(cfg.B, cfg.W, cfg.L, cfg.Hq, cfg.Hkv, cfg.D, cfg.vocab, cfg.Dh, max_ctx,
+                      dev)
+    call = lambda ev=None: step(inp["beams"], inp["q"], inp["k_draft"], inp["v_draft"],  # noqa
+                                inp["k_cache"], inp["v_cache"], inp["ctx_offsets"],
+                                inp["logits"], inp["hidden"], events=ev)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    clocks = Clocks(local).start()
+    time.sleep(0.3)
+    t0.record(stream)
+    for k in range(K):
+        call(evs[k])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    if pg:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / K
+    kern_us = {name: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K)) * 1e3
+               for i, name in enumerate(("rd_pack_beams", "rd_tree_attention", "rd_greedy_accept",
+                                          "rd_unpack"))}
+    status = int(step.status.item())
+    if status != 0:
+        raise SystemExit(f"device status {status} after the timed steps")
+
+    packed_len = step.pk["packed_len"].cpu().numpy()
+    n_acc = step.acc["n_accepted"].cpu().numpy()
+    draft_tokens = cfg.B * cfg.W * cfg.L
+    value = world * 1e3 / ms_step
+    attn_bytes = attention_bytes(cfg, inp["ctx_lens"], packed_len)
+    attn_s = kern_us["rd_tree_attention"] * 1e-6
+    peak, peak_kind = _peak_hbm()
+    achieved = attn_bytes / attn_s / 1e9
+    roofline = {"bound": "hbm", "kernel": "rd_tree_attention", "achieved": achieved,
+                "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s",
+                "traffic": _profile_traffic(cfg.name),
+                "algorithmic_bytes_per_launch": attn_bytes}
+
+    # ---- end to end through the public API, host buffers ----------------------
+    e2e = None
+    if not args.no_e2e and args.e2e_steps > 0:
+        names = ("beams", "q", "k_draft", "v_draft", "logits", "hidden")
+        host = {n: torch.empty_like(inp[n], device="cpu").pin_memory() for n in names}
+        for n in names:
+            host[n].copy_(inp[n])
+        devbuf = {n: torch.empty_like(inp[n]) for n in names}
+        outs = ("out_tokens", "n_accepted", "best_beam")
+        host_out = {n: torch.empty_like(step.acc[n], device="cpu").pin_memory() for n in outs}
+        h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+        d2h = sum(host_out[n].numel() * host_out[n].element_size() for n in outs)
+
+        def e2e_step():
+            for n in names:
+                devbuf[n].copy_(host[n], non_blocking=True)
+            step(devbuf["beams"], devbuf["q"], devbuf["k_draft"], devbuf["v_draft"],
+                 inp["k_cache"], inp["v_cache"], inp["ctx_offsets"], devbuf["logits"],
+                 devbuf["hidden"])
+            for n in outs:
+                host_out[n].copy_(step.acc[n], non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(3):
+            e2e_step()
+        if pg:
+            pg.barrier()
+        w0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        wall = time.perf_counter() - w0
+        if pg:
+            t = torch.tensor([wall], device=dev, dtype=torch.float64)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            wall = float(t.item())
+        e2e = {"value": world * args.e2e_steps / wall, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h,
+               "note": "per-step inputs (beams, q/k/v of the drafts, logits, hidden) copied from "
+                       "pinned host memory and accepted tokens read back every step; the KV "
+                       "cache is resident state"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n_req = args.cpu_sample_requests
+        dt, frac, threads = oracle_sample_time(inp, n_req)
+        cpu = {"value": frac / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"first {max(1, min(n_req, cfg.B))} of {cfg.B} requests of one step "
+                         f"(pack, tree attention, greedy accept, unpack), {dt:.1f} s, scaled "
+                         f"to a full step"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": cfg.name, "B": cfg.B, "W": cfg.W, "L": cfg.L, "Hq": cfg.Hq,
+                       "Hkv": cfg.Hkv, "D": cfg.D, "context": max_ctx, "vocab": cfg.vocab,
+                       "Dh": cfg.Dh, "l2": "inputs larger than L2 (KV cache "
+                       f"{inp['k_cache'].numel() * 4 / 1e9:.1f} GB)",
+                       "parallelism": f"replicas x{world}"},
+            "draft_tokens_per_s": value * draft_tokens,
+            "packed_tokens_per_s": world * 1e3 / ms_step * float(packed_len.sum()),
+            "dedup_pct": 100.0 * (1.0 - packed_len.sum() / draft_tokens),
+            "mean_accepted": float(n_acc.mean()),
+            "kernel_us": kern_us,
+            "tree_attention_gbs": achieved,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 4 * K,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+def main():
+    args = _args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

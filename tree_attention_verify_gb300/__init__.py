@@ -1,0 +1,244 @@
+"""Python binding of librd, the GB300 verification step of ReDrafter-style
+speculative decoding (prefix-trie packing, tree attention, greedy acceptance,
+unpack).
+
+The binding only marshals arguments: it checks tensor shapes, dtypes, devices
+and contiguity, allocates outputs with torch when the caller passes none, and
+calls the C ABI declared in include/rd.h on the current CUDA stream.  Every step
+of the computation runs in the CUDA kernels of librd.so.  There is no CPU path:
+if the library cannot be loaded, importing this package raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "rd_pack_beams", "rd_tree_attention", "rd_tree_attention_workspace_size",
+    "rd_causal_attention", "rd_unpack", "rd_greedy_accept",
+    "rd_greedy_accept_workspace_size", "RdError", "DEV_BAD_INDEX", "DEV_BAD_TOKEN",
+    "DEV_OVERFLOW", "DEV_BAD_LENGTH", "DEV_TIMEOUT", "lib_path",
+]
+
+DEV_BAD_INDEX, DEV_BAD_TOKEN, DEV_OVERFLOW, DEV_BAD_LENGTH, DEV_TIMEOUT = 1, 2, 4, 8, 16
+RD_OK, RD_ERR_INVALID_ARG, RD_ERR_UNSUPPORTED, RD_ERR_CUDA = 0, 1, 2, 3
+_DTYPES = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2, torch.int32: 3}
+
+
+class RdError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {_lib.rd_status_string(status).decode()} ({status})")
+
+
+def _load() -> ctypes.CDLL:
+    path = _build.LIB
+    if _build.needs_build():
+        _build.build()
+    if not os.path.exists(path):
+        raise ImportError(f"librd.so missing at {path}; build it with __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    P, I, I64, F, S = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                       ctypes.c_size_t)
+    sig = {
+        "rd_pack_beams": [P, I, I, I, I, P, P, P, P, P, P, P, P],
+        "rd_tree_attention_workspace_size": [I, I, I, I, I, I],
+        "rd_tree_attention": [I, I, I, I, I, F, P, P, P, P, P, P, I64, I, P, P, I, P, P, S,
+                              P, P],
+        "rd_causal_attention": [I, I, I, I, F, P, P, P, P, I64, I, P, P, P],
+        "rd_unpack": [P, I, I, I, I, P, I, I, P, P, P],
+        "rd_greedy_accept_workspace_size": [I, I, I],
+        "rd_greedy_accept": [P, I, I, I, P, P, P, I, I, P, P, P, P, P, P, S, P, P],
+    }
+    for name, args in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = S if name.endswith("workspace_size") else I
+    lib.rd_status_string.argtypes = [I]
+    lib.rd_status_string.restype = ctypes.c_char_p
+    return lib
+
+
+_lib = _load()
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+# ----------------------------------------------------------------------------
+# marshalling helpers
+# ----------------------------------------------------------------------------
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, device=None, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+
+
+def _check(fn: str, status: int):
+    if status != RD_OK:
+        raise RdError(fn, status)
+
+
+def _empty(shape, dtype, like: torch.Tensor):
+    return torch.empty(shape, dtype=dtype, device=like.device)
+
+
+# ----------------------------------------------------------------------------
+# entry points (same names as the C ABI)
+# ----------------------------------------------------------------------------
+def rd_pack_beams(beams: torch.Tensor, P_cap: Optional[int] = None, *, out: Optional[dict] = None,
+                  dev_status: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """Prefix dedup of int32 beams [B, W, L].  Returns dict(tokens, packer, unpacker,
+    mask, depth, packed_len) of device tensors (see rd_pack_beams in rd.h)."""
+    _need(beams, "beams", torch.int32, ndim=3)
+    B, W, L = beams.shape
+    P_cap = W * L if P_cap is None else int(P_cap)
+    NW = (P_cap + 31) // 32
+    if out is None:
+        out = dict(tokens=_empty((B, P_cap), torch.int32, beams),
+                   packer=_empty((B, P_cap), torch.int32, beams),
+                   unpacker=_empty((B, W, L), torch.int32, beams),
+                   mask=_empty((B, P_cap, NW), torch.int32, beams),   # uint32 bit rows
+                   depth=_empty((B, P_cap), torch.int32, beams),
+                   packed_len=_empty((B,), torch.int32, beams))
+    _check("rd_pack_beams", _lib.rd_pack_beams(
+        _ptr(beams), B, W, L, P_cap, _ptr(out["tokens"]), _ptr(out["packer"]),
+        _ptr(out["unpacker"]), _ptr(out["mask"]), _ptr(out.get("depth")),
+        _ptr(out["packed_len"]), _ptr(dev_status), _stream(stream)))
+    return out
+
+
+def rd_tree_attention_workspace_size(B: int, P_max: int, Hq: int, Hkv: int, D: int,
+                                     max_ctx: int) -> int:
+    return int(_lib.rd_tree_attention_workspace_size(B, P_max, Hq, Hkv, D, max_ctx))
+
+
+def rd_tree_attention(q, k_new, v_new, k_cache, v_cache, ctx_offsets, packed_len, mask, *,
+                      max_ctx: int, scale: float = 0.0, out=None, workspace=None,
+                      dev_status=None, stream=None) -> torch.Tensor:
+    """Tree-masked attention of packed drafts (see rd_tree_attention in rd.h).
+    q [B,P,Hq,D], k_new/v_new [B,P,Hkv,D], k_cache/v_cache [sum C,Hkv,D] bf16;
+    ctx_offsets int64 [B+1]; packed_len int32 [B]; mask uint32/int32 [B,P,NW].
+    The workspace (if the plan needs one) must start zero-filled; it is returned
+    to zero by every call.  Pass the same workspace again to reuse it."""
+    for n, t in (("q", q), ("k_new", k_new), ("v_new", v_new)):
+        _need(t, n, torch.bfloat16, ndim=4)
+    _need(k_cache, "k_cache", torch.bfloat16, ndim=3)
+    _need(v_cache, "v_cache", torch.bfloat16, ndim=3)
+    _need(ctx_offsets, "ctx_offsets", torch.int64, ndim=1)
+    _need(packed_len, "packed_len", torch.int32, ndim=1)
+    if mask.dim() != 3 or not mask.is_contiguous() or mask.element_size() != 4:
+        raise ValueError("mask must be a contiguous 32-bit [B, P_max, NW] tensor")
+    B, P, Hq, D = q.shape
+    Hkv = k_new.shape[2]
+    if k_new.shape != (B, P, Hkv, D) or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new must be [B, P_max, Hkv, D]")
+    if k_cache.shape[1:] != (Hkv, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache/v_cache must be [total_ctx, Hkv, D]")
+    if ctx_offsets.numel() != B + 1 or packed_len.numel() != B or mask.shape[:2] != (B, P):
+        raise ValueError("ctx_offsets/packed_len/mask shapes do not match q")
+    if out is None:
+        out = torch.empty_like(q)
+    ws_need = rd_tree_attention_workspace_size(B, P, Hq, Hkv, D, max_ctx)
+    if ws_need and workspace is None:
+        workspace = torch.zeros(ws_need, dtype=torch.uint8, device=q.device)
+    _check("rd_tree_attention", _lib.rd_tree_attention(
+        B, P, Hq, Hkv, D, float(scale), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+        _ptr(v_cache), _ptr(ctx_offsets), int(k_cache.shape[0]), int(max_ctx), _ptr(packed_len),
+        _ptr(mask), int(mask.shape[2]), _ptr(out), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(),
+        _ptr(dev_status), _stream(stream)))
+    return out
+
+
+def rd_causal_attention(q, k, v, cu_seqlens, *, max_seqlen: int, scale: float = 0.0,
+                        out=None, dev_status=None, stream=None) -> torch.Tensor:
+    """Causal prefill attention: q [T,Hq,D], k/v [T,Hkv,D] bf16, cu_seqlens int32 [B+1]."""
+    _need(q, "q", torch.bfloat16, ndim=3)
+    _need(k, "k", torch.bfloat16, ndim=3)
+    _need(v, "v", torch.bfloat16, ndim=3)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, ndim=1)
+    T, Hq, D = q.shape
+    if k.shape[0] != T or v.shape != k.shape or k.shape[2] != D:
+        raise ValueError("k/v must be [T, Hkv, D] with the rows of q")
+    if out is None:
+        out = torch.empty_like(q)
+    _check("rd_causal_attention", _lib.rd_causal_attention(
+        cu_seqlens.numel() - 1, Hq, k.shape[1], D, float(scale), _ptr(q), _ptr(k), _ptr(v),
+        _ptr(cu_seqlens), T, int(max_seqlen), _ptr(out), _ptr(dev_status), _stream(stream)))
+    return out
+
+
+def rd_unpack(packed: torch.Tensor, unpacker: torch.Tensor, *, out=None, dev_status=None,
+              stream=None) -> torch.Tensor:
+    """out[b,w,i,:] = packed[b, unpacker[b,w,i], :] (exact copy)."""
+    if packed.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {packed.dtype}")
+    _need(packed, "packed", packed.dtype, ndim=3)
+    _need(unpacker, "unpacker", torch.int32, ndim=3)
+    B, P, Dh = packed.shape
+    _, W, L = unpacker.shape
+    if unpacker.shape[0] != B:
+        raise ValueError("unpacker batch does not match packed")
+    if out is None:
+        out = _empty((B, W, L, Dh), packed.dtype, packed)
+    _check("rd_unpack", _lib.rd_unpack(_ptr(packed), _DTYPES[packed.dtype], B, P, Dh,
+                                       _ptr(unpacker), W, L, _ptr(out), _ptr(dev_status),
+                                       _stream(stream)))
+    return out
+
+
+def rd_greedy_accept_workspace_size(B: int, P_max: int, V: int) -> int:
+    return int(_lib.rd_greedy_accept_workspace_size(B, P_max, V))
+
+
+def rd_greedy_accept(logits, beams, unpacker, packed_len, *, out=None, workspace=None,
+                     dev_status=None, stream=None) -> dict:
+    """Greedy verification (see rd_greedy_accept in rd.h).  Returns dict(argmax,
+    accept_len, best_beam, n_accepted, out_tokens).  The workspace must start
+    zero-filled; every call leaves it zeroed."""
+    _need(logits, "logits", torch.bfloat16, ndim=3)
+    _need(beams, "beams", torch.int32, ndim=3)
+    _need(unpacker, "unpacker", torch.int32, ndim=3)
+    _need(packed_len, "packed_len", torch.int32, ndim=1)
+    B, P, V = logits.shape
+    _, W, L = beams.shape
+    if out is None:
+        out = dict(argmax=_empty((B, P), torch.int32, logits),
+                   accept_len=_empty((B, W), torch.int32, logits),
+                   best_beam=_empty((B,), torch.int32, logits),
+                   n_accepted=_empty((B,), torch.int32, logits),
+                   out_tokens=_empty((B, L), torch.int32, logits))
+    if workspace is None:
+        workspace = torch.zeros(max(8, rd_greedy_accept_workspace_size(B, P, V)),
+                                dtype=torch.uint8, device=logits.device)
+    _check("rd_greedy_accept", _lib.rd_greedy_accept(
+        _ptr(logits), B, P, V, _ptr(beams), _ptr(unpacker), _ptr(packed_len), W, L,
+        _ptr(out["argmax"]), _ptr(out["accept_len"]), _ptr(out["best_beam"]),
+        _ptr(out["n_accepted"]), _ptr(out["out_tokens"]), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream)))
+    return out

@@ -1,0 +1,58 @@
+// Internal helpers shared by the librd kernels (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "rd.h"
+
+#define RD_WARP 32
+
+// OR error bits into the caller's device status word; never traps.
+__device__ __forceinline__ void rd_flag(int32_t* status, unsigned bits)
+{
+    if (status != nullptr) atomicOr(reinterpret_cast<int*>(status), static_cast<int>(bits));
+}
+
+// Launchers (one per kernel family), called by the C entry points in rd_api.cu
+// after host-side validation.  Each returns the cudaGetLastError() of its launches.
+cudaError_t rd_launch_pack(const int32_t* beams, int B, int W, int L, int P_cap,
+                           int32_t* tokens, int32_t* packer, int32_t* unpacker,
+                           uint32_t* mask, int32_t* depth, int32_t* packed_len,
+                           int32_t* dev_status, cudaStream_t stream);
+
+cudaError_t rd_launch_unpack(const void* packed, int esize, int B, int P_max, int Dh,
+                             const int32_t* unpacker, int W, int L, void* out,
+                             int32_t* dev_status, cudaStream_t stream);
+
+struct rd_accept_plan {
+    int splits;        // vocab chunks per packed row
+    int chunk;         // elements per chunk (multiple of 8)
+};
+rd_accept_plan rd_accept_make_plan(int B, int P_max, int V);
+size_t rd_accept_workspace_bytes(int B, int P_max);
+cudaError_t rd_launch_greedy_accept(const void* logits, int B, int P_max, int V,
+                                    const int32_t* beams, const int32_t* unpacker,
+                                    const int32_t* packed_len, int W, int L,
+                                    int32_t* argmax, int32_t* accept_len,
+                                    int32_t* best_beam, int32_t* n_accepted,
+                                    int32_t* out_tokens, void* workspace,
+                                    int32_t* dev_status, cudaStream_t stream);
+
+// Attention (tree and causal modes share one kernel family).
+struct rd_attn_plan {
+    int tiles;         // row tiles per (request, kv head)
+    int splits;        // KV splits per (request, kv head, tile), grid upper bound
+    int split_len;     // KV positions per split (multiple of the chunk size)
+    size_t ws_bytes;   // workspace bytes needed
+};
+rd_attn_plan rd_attn_make_plan(bool causal, int B, int P_max, int Hq, int Hkv, int D,
+                               int max_kv);
+cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, int P_max,
+                                int Hq, int Hkv, int D, float scale, const void* q,
+                                const void* k_new, const void* v_new,
+                                const void* k_cache, const void* v_cache,
+                                const int64_t* ctx_offsets, int64_t total_kv, int max_kv,
+                                const int32_t* lens, const uint32_t* mask, int mask_words,
+                                void* o, void* workspace, int32_t* dev_status,
+                                cudaStream_t stream);
