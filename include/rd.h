@@ -218,6 +218,38 @@ rd_status rd_greedy_accept(const void* logits, int B, int P_max, int V,
                            void* workspace, size_t ws_bytes,
                            int32_t* dev_status, rd_stream_t stream);
 
+/*
+ * rd_greedy_accept_noalloc -- rd_greedy_accept for callers that cannot
+ * allocate device memory.  The pages have no counterpart: this is a library
+ * convenience, not part of the method.
+ *
+ * Same arguments and results as rd_greedy_accept, without the workspace.  Some
+ * callers cannot call cudaMalloc on the serving path (a plugin inside a host
+ * framework that owns all device memory, a runtime that must not allocate after
+ * start-up because an allocation can synchronise the device or fail under
+ * memory pressure).  This entry point takes its scratch from a fixed array in
+ * device global memory that the library owns: about 768 KB, held on every GPU
+ * that loads librd until the process exits.
+ *  - Limits: B * P_max <= 65536 and B <= 65535; beyond them it returns
+ *    RD_ERR_UNSUPPORTED without launching.
+ *  - It allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ *    routine.  It clears the part of the array it uses with cudaMemsetAsync on
+ *    `stream` before its kernel.
+ *  - Every call on a device shares the one array: calls whose work overlaps on
+ *    the GPU (different streams or host threads without ordering) race and
+ *    give wrong results.  Order them on one stream.
+ *  - The first call on a device looks the array's device address up with that
+ *    device current (cudaGetSymbolAddress); make that first call before any
+ *    stream capture begins.
+ */
+rd_status rd_greedy_accept_noalloc(const void* logits, int B, int P_max, int V,
+                                   const int32_t* beams, const int32_t* unpacker,
+                                   const int32_t* packed_len, int W, int L,
+                                   int32_t* argmax, int32_t* accept_len,
+                                   int32_t* best_beam, int32_t* n_accepted,
+                                   int32_t* out_tokens, int32_t* dev_status,
+                                   rd_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

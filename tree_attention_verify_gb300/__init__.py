@@ -21,7 +21,7 @@ from . import _build
 __all__ = [
     "rd_pack_beams", "rd_tree_attention", "rd_tree_attention_workspace_size",
     "rd_causal_attention", "rd_unpack", "rd_greedy_accept",
-    "rd_greedy_accept_workspace_size", "RdError", "DEV_BAD_INDEX", "DEV_BAD_TOKEN",
+    "rd_greedy_accept_workspace_size", "rd_greedy_accept_noalloc", "RdError", "DEV_BAD_INDEX", "DEV_BAD_TOKEN",
     "DEV_OVERFLOW", "DEV_BAD_LENGTH", "DEV_TIMEOUT", "lib_path",
 ]
 
@@ -54,6 +54,7 @@ def _load() -> ctypes.CDLL:
         "rd_unpack": [P, I, I, I, I, P, I, I, P, P, P],
         "rd_greedy_accept_workspace_size": [I, I, I],
         "rd_greedy_accept": [P, I, I, I, P, P, P, I, I, P, P, P, P, P, P, S, P, P],
+        "rd_greedy_accept_noalloc": [P, I, I, I, P, P, P, I, I, P, P, P, P, P, P, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -241,4 +242,29 @@ def rd_greedy_accept(logits, beams, unpacker, packed_len, *, out=None, workspace
         _ptr(out["argmax"]), _ptr(out["accept_len"]), _ptr(out["best_beam"]),
         _ptr(out["n_accepted"]), _ptr(out["out_tokens"]), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream)))
+    return out
+
+
+def rd_greedy_accept_noalloc(logits, beams, unpacker, packed_len, *, out=None, dev_status=None,
+                             stream=None) -> dict:
+    """rd_greedy_accept without a caller workspace, for callers that cannot allocate
+    device memory: the scratch is a fixed array inside librd shared by every call
+    on the device, so calls must not overlap on the GPU.  Limits: B * P_max <= 65536.
+    (The outputs are allocated here only when `out` is not given.)"""
+    _need(logits, "logits", torch.bfloat16, ndim=3)
+    _need(beams, "beams", torch.int32, ndim=3)
+    _need(unpacker, "unpacker", torch.int32, ndim=3)
+    _need(packed_len, "packed_len", torch.int32, ndim=1)
+    B, P, V = logits.shape
+    _, W, L = beams.shape
+    if out is None:
+        out = dict(argmax=_empty((B, P), torch.int32, logits),
+                   accept_len=_empty((B, W), torch.int32, logits),
+                   best_beam=_empty((B,), torch.int32, logits),
+                   n_accepted=_empty((B,), torch.int32, logits),
+                   out_tokens=_empty((B, L), torch.int32, logits))
+    _check("rd_greedy_accept_noalloc", _lib.rd_greedy_accept_noalloc(
+        _ptr(logits), B, P, V, _ptr(beams), _ptr(unpacker), _ptr(packed_len), W, L,
+        _ptr(out["argmax"]), _ptr(out["accept_len"]), _ptr(out["best_beam"]),
+        _ptr(out["n_accepted"]), _ptr(out["out_tokens"]), _ptr(dev_status), _stream(stream)))
     return out
