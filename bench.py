@@ -75,6 +75,20 @@ def _dist():
     return world, rank, local
 
 
+def rank_seed(cfg, rank: int) -> int:
+    """Each rank verifies its own batch (weak scaling): its inputs use this seed."""
+    return cfg.seed + 1000 * rank
+
+
+def max_over_ranks(x: float, dist=None, device=None) -> float:
+    """The slowest rank's value (the only collective besides the barrier)."""
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _peak_hbm():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -255,7 +269,7 @@ def run_ours(args):
         pg = dist
 
     cfg = _config(args)
-    inp = workloads.make_verify_inputs(cfg, device=dev, seed=cfg.seed + 1000 * rank)
+    inp = workloads.make_verify_inputs(cfg, device=dev, seed=rank_seed(cfg, rank))
     max_ctx = int(inp["ctx_lens"].max())
     step = VerifyStep(cfg.B, cfg.W, cfg.L, cfg.Hq, cfg.Hkv, cfg.D, cfg.vocab, cfg.Dh, max_ctx,
                       dev)
@@ -284,11 +298,7 @@ def run_ours(args):
     if pg:
         pg.barrier()
     clk = clocks.stop()
-    ms = t0.elapsed_time(t1)
-    if pg:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(t0.elapsed_time(t1), pg, dev)
     ms_step = ms / K
     kern_us = {name: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K)) * 1e3
                for i, name in enumerate(("rd_pack_beams", "rd_tree_attention", "rd_greedy_accept",
@@ -342,11 +352,7 @@ def run_ours(args):
         w0 = time.perf_counter()
         for _ in range(args.e2e_steps):
             e2e_step()
-        wall = time.perf_counter() - w0
-        if pg:
-            t = torch.tensor([wall], device=dev, dtype=torch.float64)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            wall = float(t.item())
+        wall = max_over_ranks(time.perf_counter() - w0, pg, dev)
         e2e = {"value": world * args.e2e_steps / wall, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h,
                "note": "per-step inputs (beams, q/k/v of the drafts, logits, hidden) copied from "
