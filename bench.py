@@ -38,7 +38,7 @@ import workloads  # noqa: E402
 METRIC = "verify_steps_per_s"
 UNIT = "steps/s"
 FALLBACK_HBM_GBS = 6800.0
-ATTN_SRC = os.path.join(ROOT, "tree_attention_verify_gb300", "csrc", "attention_mma.cu")
+ATTN_SRC = os.path.join(ROOT, "tree_attention_verify_gb300", "csrc", "attention_tc.cu")
 
 
 # ----------------------------------------------------------------------------
@@ -52,7 +52,7 @@ def _args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="13b_b64", choices=list(workloads.CONFIGS))
     ap.add_argument("--e2e-steps", type=int, default=30)
-    ap.add_argument("--cpu-sample-requests", type=int, default=4)
+    ap.add_argument("--cpu-sample-requests", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=0,

@@ -1,0 +1,735 @@
+// Tree attention (generation phase) and causal prefill (context phase) on the
+// 5th-generation tensor cores: TMA-fed, tcgen05 MMA with TMEM accumulators,
+// warp-specialised, persistent.
+//
+// A single kernel with a topology-aware mask verifies every candidate path at
+// once (speculative-decoding survey page, SpecInfer "Token Tree Verifier"), and
+// TensorRT-LLM's attention plugin splits context and generation requests
+// (NVIDIA blog "ReDrafter in TensorRT-LLM", section "Inflight-batching
+// Compatible Engine").
+//
+// Work unit = (request b, kv head h, 128-row query tile, KV split).  The G query
+// heads that share kv head h are stacked as rows (row r -> node p = r / G, head
+// h*G + r % G; causal: token t = r / G), so each K/V byte is read once per tile.
+// Row r of a tile is TMEM lane r.  A unit walks its KV chunks of 64 positions:
+// first the context (all visible; the last chunk is ragged), then the packed
+// drafts (visible iff the node's ancestor-mask bit is set).
+//
+// Warp roles (192 threads, one CTA per SM, persistent over units):
+//   warps 0-3  softmax: TMEM lane = row.  Load the tile's queries into shared
+//              memory, turn S into bf16 probabilities P (online softmax in exp2
+//              form, rescaling O in TMEM only when a row maximum grows by more
+//              than 2^8), and write the output rows.
+//   warp 4     producer: TMA loads of K and V chunks (128-byte swizzle) into a
+//              ring of stages.
+//   warp 5     MMA issuer: S = Q K^T (M=128, N=64, K=D) into a double-buffered
+//              TMEM tile, then O += P V (M=128, N=D, K=64) into TMEM.
+// Every wait is bounded by a clock budget; on expiry the CTA records
+// RD_DEV_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "rd_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace {
+using namespace rdtc;
+
+constexpr int kM = 128;                    // query rows per tile = TMEM lanes
+constexpr int kN = 64;                     // KV positions per chunk
+constexpr int kSoftmaxThreads = 128;
+constexpr int kThreads = kSoftmaxThreads + 64;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when a max grows by > 2^8
+constexpr long long kWaitBudget = 4000000000LL;   // ~2 s of SM clock per wait
+
+template <int D> struct Cfg {
+    static constexpr int kDB = D / 64;                  // 64-element (128-byte) column blocks
+    static constexpr int kStages = D == 128 ? 5 : 8;
+    static constexpr int kQBytes = kM * D * 2;
+    static constexpr int kPBytes = kM * kN * 2;         // one probability buffer
+    static constexpr int kKBytes = kN * D * 2;          // one K (or V) chunk
+    static constexpr int kStageBytes = 2 * kKBytes;
+    static constexpr int kQOff = 0;
+    static constexpr int kPOff = kQOff + kQBytes;
+    static constexpr int kStageOff = kPOff + 2 * kPBytes;
+    static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
+    static constexpr int kSmemBytes = kBarOff + 256 + 1024;   // + barriers + alignment slack
+    static constexpr uint32_t kTmemCols = 256;          // S: 2 x 64, O: D (<= 128)
+    static constexpr uint32_t kSCol = 0;
+    static constexpr uint32_t kOCol = 128;
+};
+
+struct TcArgs {
+    bool causal;
+    int B, P_max, Hq, Hkv, G, tiles, splits, chunks_per_split, mask_words, n_units;
+    float scale_log2;
+    const uint16_t* q;
+    const int64_t* ctx_offsets;
+    int64_t total_kv;
+    int max_kv;
+    const int32_t* lens;
+    const uint32_t* mask;
+    uint16_t* o;
+    float* o_part;
+    float2* ml_part;
+    unsigned int* tickets;
+    int32_t* status;
+};
+
+struct Barriers {
+    uint64_t kv_full[8];
+    uint64_t kv_empty[8];
+    uint64_t s_full[2];
+    uint64_t s_free[2];
+    uint64_t p_full[2];
+    uint64_t pv_done;
+    uint64_t o_final;
+    uint64_t q_full;
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+// Geometry of one work unit, computed identically by every role.
+struct UnitGeo {
+    int b, h, tile, split;
+    bool live;            // has valid rows and this split exists
+    bool zero_tile;       // tree tile without valid rows: write zeros (split 0 only)
+    int n_rows;           // valid rows of (b, h)
+    int64_t kv_base;      // first row of this request / sequence in the K/V map
+    int C;                // context length (tree) or sequence length (causal)
+    int Pb;               // packed length (tree)
+    int c_first, n_ctx;   // first context chunk and number of context chunks
+    int n_draft;          // draft chunks (last split only)
+    int n_splits;
+};
+
+__device__ __forceinline__ UnitGeo unit_geo(const TcArgs& a, int u)
+{
+    UnitGeo g;
+    const int per_bh = a.tiles * a.splits;
+    g.b = u / (a.Hkv * per_bh);
+    const int rem = u % (a.Hkv * per_bh);
+    g.h = rem / per_bh;
+    g.tile = (rem % per_bh) / a.splits;
+    g.split = rem % a.splits;
+    g.live = false;
+    g.zero_tile = false;
+    g.n_draft = 0;
+    g.n_ctx = 0;
+    g.c_first = 0;
+    g.n_splits = 1;
+    bool bad;
+    if (a.causal) {
+        const int s0 = a.lens[g.b], s1 = a.lens[g.b + 1];
+        g.kv_base = s0;
+        g.C = s1 - s0;
+        g.Pb = 0;
+        bad = s0 < 0 || g.C < 0 || g.C > a.max_kv || s1 > a.total_kv;
+        if (bad) g.C = 0;
+        g.n_rows = g.C * a.G;
+        const int row0 = g.tile * kM;
+        if (row0 < g.n_rows && g.split == 0) {
+            const int t_max = (min(g.n_rows, row0 + kM) - 1) / a.G;
+            g.n_ctx = t_max / kN + 1;
+            g.live = true;
+        }
+    } else {
+        const int64_t c0 = a.ctx_offsets[g.b], c1 = a.ctx_offsets[g.b + 1];
+        g.kv_base = c0;
+        g.C = (int)(c1 - c0);
+        g.Pb = a.lens[g.b];
+        bad = c0 < 0 || c1 < c0 || c1 - c0 > a.max_kv || c1 > a.total_kv || g.Pb < 0 ||
+              g.Pb > a.P_max;
+        if (bad) { g.C = 0; g.Pb = 0; }
+        g.n_rows = g.Pb * a.G;
+        const int row0 = g.tile * kM;
+        const int n_cc = (g.C + kN - 1) / kN;
+        g.n_splits = max(1, (n_cc + a.chunks_per_split - 1) / a.chunks_per_split);
+        if (row0 >= g.n_rows) {
+            g.zero_tile = g.split == 0 && row0 < a.P_max * a.G;
+        } else if (g.split < g.n_splits) {
+            g.live = true;
+            g.c_first = g.split * a.chunks_per_split;
+            g.n_ctx = max(0, min(n_cc, g.c_first + a.chunks_per_split) - g.c_first);
+            if (g.split == g.n_splits - 1) g.n_draft = (g.Pb + kN - 1) / kN;
+        }
+    }
+    if (bad && g.h == 0 && g.tile == 0 && g.split == 0 && threadIdx.x == 0)
+        rd_flag(a.status, RD_DEV_BAD_LENGTH);
+    return g;
+}
+
+// 16-byte chunk c of row r in a [rows][128 B] tile with the 128-byte swizzle
+__device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 2^x with the hardware approximation (ex2.approx; 2^-inf = 0)
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Warp-uniform bounded wait: every lane waits, and the warp fails as one if any
+// lane ran out of budget or saw the abort flag.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          long long budget)
+{
+    const bool ok = mbar_wait(bar, parity, abort, budget);
+    return __all_sync(0xffffffffu, ok);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map_kc,
+                         const __grid_constant__ CUtensorMap map_vc,
+                         const __grid_constant__ CUtensorMap map_kd,
+                         const __grid_constant__ CUtensorMap map_vd)
+{
+    using C = Cfg<D>;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Barriers& bar = *reinterpret_cast<Barriers*>(smem + C::kBarOff);
+    __shared__ int s_last;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    volatile int* abort = &bar.abort;
+    volatile int no_abort = 0;
+
+    if (tid == 0) {
+        for (int i = 0; i < C::kStages; ++i) {
+            mbar_init(&bar.kv_full[i], 1);
+            mbar_init(&bar.kv_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar.s_full[i], 1);
+            mbar_init(&bar.s_free[i], 4);
+            mbar_init(&bar.p_full[i], 4);
+        }
+        mbar_init(&bar.pv_done, 1);
+        mbar_init(&bar.o_final, 1);
+        mbar_init(&bar.q_full, 4);
+        mbar_init(&bar.drain, 1);
+        bar.abort = 0;
+        mbar_fence_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&bar.tmem_base, C::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        tma_prefetch_desc(&map_kc);
+        tma_prefetch_desc(&map_vc);
+        tma_prefetch_desc(&map_kd);
+        tma_prefetch_desc(&map_vd);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bar.tmem_base;
+
+    auto fail = [&]() {
+        *abort = 1;
+        rd_flag(a.status, RD_DEV_TIMEOUT);
+    };
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            uint32_t g = 0;                               // global chunk counter
+            for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
+                const UnitGeo geo = unit_geo(a, u);
+                if (!geo.live) continue;
+                const int n = geo.n_ctx + geo.n_draft;
+                for (int j = 0; j < n; ++j, ++g) {
+                    const int st = g % C::kStages;
+                    if (g >= (uint32_t)C::kStages &&
+                        !mbar_wait(&bar.kv_empty[st], ((g / C::kStages) - 1) & 1, abort,
+                                   kWaitBudget)) { fail(); break; }
+                    unsigned char* ks = smem + C::kStageOff + st * C::kStageBytes;
+                    unsigned char* vs = ks + C::kKBytes;
+                    mbar_arrive_expect_tx(&bar.kv_full[st], C::kStageBytes);
+                    const CUtensorMap* mk;
+                    const CUtensorMap* mv;
+                    int z;
+                    if (j < geo.n_ctx) {
+                        mk = &map_kc; mv = &map_vc;
+                        z = (int)(geo.kv_base + (int64_t)(geo.c_first + j) * kN);
+                    } else {
+                        mk = &map_kd; mv = &map_vd;
+                        z = geo.b * a.P_max + (j - geo.n_ctx) * kN;
+                    }
+#pragma unroll
+                    for (int db = 0; db < C::kDB; ++db) {
+                        tma_load_3d(ks + db * (kN * 128), mk, &bar.kv_full[st], db * 64, geo.h, z);
+                        tma_load_3d(vs + db * (kN * 128), mv, &bar.kv_full[st], db * 64, geo.h, z);
+                    }
+                }
+            }
+            // drain: every issued copy must land before the CTA may exit
+            const uint32_t first = g > (uint32_t)C::kStages ? g - C::kStages : 0u;
+            for (uint32_t k = first; k < g; ++k)
+                mbar_wait(&bar.kv_full[k % C::kStages], (k / C::kStages) & 1, &no_abort, kWaitBudget);
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_bf16(kM, kN, false, false);
+            constexpr uint32_t idPV = idesc_bf16(kM, D, false, true);
+            const uint32_t q_base = smem_addr(smem + C::kQOff);
+            uint32_t g = 0, unit_iter = 0;
+            auto issue_pv = [&](uint32_t gp, int jp) -> bool {
+                const int sb = gp & 1;
+                if (!mbar_wait(&bar.p_full[sb], (gp >> 1) & 1, abort, kWaitBudget)) return false;
+                tc_fence_after();
+                const uint32_t p_base = smem_addr(smem + C::kPOff + sb * C::kPBytes);
+                const uint32_t v_base =
+                    smem_addr(smem + C::kStageOff + (gp % C::kStages) * C::kStageBytes + C::kKBytes);
+#pragma unroll
+                for (int kk = 0; kk < kN / 16; ++kk) {
+                    const uint64_t ad = smem_desc(p_base + kk * 32, 16, 1024, kSwizzle128B);
+                    const uint64_t bd = smem_desc(v_base + kk * 2048, kN * 128, 1024, kSwizzle128B);
+                    mma_bf16(tmem + C::kOCol, ad, bd, idPV, jp > 0 || kk > 0);
+                }
+                mma_commit(&bar.kv_empty[gp % C::kStages]);
+                mma_commit(&bar.pv_done);
+                return true;
+            };
+            for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
+                const UnitGeo geo = unit_geo(a, u);
+                if (!geo.live) continue;
+                const int n = geo.n_ctx + geo.n_draft;
+                if (!mbar_wait(&bar.q_full, unit_iter & 1, abort, kWaitBudget)) { fail(); break; }
+                tc_fence_after();
+                bool ok = true;
+                for (int j = 0; j < n && ok; ++j) {
+                    const uint32_t gg = g + j;
+                    const int st = gg % C::kStages;
+                    const int sb = gg & 1;
+                    if (!mbar_wait(&bar.kv_full[st], (gg / C::kStages) & 1, abort, kWaitBudget)) { ok = false; break; }
+                    if (gg >= 2 && !mbar_wait(&bar.s_free[sb], ((gg >> 1) - 1) & 1, abort, kWaitBudget)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t k_base = smem_addr(smem + C::kStageOff + st * C::kStageBytes);
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint32_t koff = (ks >> 2) * (kN * 128) + (ks & 3) * 32;
+                        const uint32_t qoff = (ks >> 2) * (kM * 128) + (ks & 3) * 32;
+                        const uint64_t ad = smem_desc(q_base + qoff, 16, 1024, kSwizzle128B);
+                        const uint64_t bd = smem_desc(k_base + koff, 16, 1024, kSwizzle128B);
+                        mma_bf16(tmem + C::kSCol + sb * kN, ad, bd, idS, ks > 0);
+                    }
+                    mma_commit(&bar.s_full[sb]);
+                    if (j >= 1 && !issue_pv(gg - 1, j - 1)) { ok = false; break; }
+                }
+                if (ok && !issue_pv(g + n - 1, n - 1)) ok = false;
+                if (!ok) { fail(); break; }
+                mma_commit(&bar.o_final);
+                g += n;
+                ++unit_iter;
+            }
+            // drain: every issued MMA must finish before TMEM is freed
+            mma_commit(&bar.drain);
+            mbar_wait(&bar.drain, 0, &no_abort, kWaitBudget);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int t = tid;                                 // row within the tile = TMEM lane
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        uint32_t g = 0, unit_iter = 0;
+        for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
+            const UnitGeo geo = unit_geo(a, u);
+            const int row = geo.tile * kM + t;
+            const int hq0 = geo.h * a.G;
+            if (geo.zero_tile) {                           // padded rows of a tree tile
+                const int p = row / a.G;
+                if (p < a.P_max) {
+                    uint4* dst = reinterpret_cast<uint4*>(
+                        a.o + (((size_t)geo.b * a.P_max + p) * a.Hq + hq0 + row % a.G) * D);
+#pragma unroll
+                    for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+                }
+                continue;
+            }
+            if (!geo.live) continue;
+            const int n = geo.n_ctx + geo.n_draft;
+            const bool valid = row < geo.n_rows;
+            const int qpos = row / a.G;                    // node p (tree) / token t (causal)
+            // ---- queries -> shared memory (128-byte swizzle, K-major) ----------
+            {
+                const uint4* src = nullptr;
+                if (valid) {
+                    const size_t qrow = a.causal ? (size_t)(geo.kv_base + qpos)
+                                                 : (size_t)geo.b * a.P_max + qpos;
+                    src = reinterpret_cast<const uint4*>(a.q + (qrow * a.Hq + hq0 + row % a.G) * D);
+                }
+                unsigned char* qs = smem + C::kQOff;
+#pragma unroll
+                for (int c = 0; c < D / 8; ++c) {
+                    const uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4*>(qs + (c >> 3) * (kM * 128) + sw128(t, c & 7)) = v;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar.q_full);
+            }
+            float m = -INFINITY, l = 0.f;
+            const uint32_t* mrow = (!a.causal && valid)
+                ? a.mask + ((size_t)geo.b * a.P_max + qpos) * a.mask_words : nullptr;
+            bool ok = true;
+            for (int j = 0; j < n; ++j) {
+                const uint32_t gg = g + j;
+                const int sb = gg & 1;
+                if (!warp_wait(&bar.s_full[sb], (gg >> 1) & 1, abort, kWaitBudget)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t sr[64];
+                tmem_ld32(tmem + lane_base + C::kSCol + sb * kN, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+                tmem_ld32(tmem + lane_base + C::kSCol + sb * kN + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar.s_free[sb]);
+                float s[64];
+#pragma unroll
+                for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c]);
+                // ---- visibility -----------------------------------------------
+                if (!valid) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) s[c] = -INFINITY;
+                } else if (j < geo.n_ctx) {
+                    const int pos0 = (geo.c_first + j) * kN;
+                    const int lim = a.causal ? min(geo.C, qpos + 1) : geo.C;   // visible: pos < lim
+                    if (pos0 + kN > lim) {
+#pragma unroll
+                        for (int c = 0; c < 64; ++c)
+                            if (pos0 + c >= lim) s[c] = -INFINITY;
+                    }
+                } else {
+                    const int d0 = (j - geo.n_ctx) * kN;
+                    const uint32_t w0 = (d0 >> 5) < a.mask_words ? __ldg(mrow + (d0 >> 5)) : 0u;
+                    const uint32_t w1 = (d0 >> 5) + 1 < a.mask_words ? __ldg(mrow + (d0 >> 5) + 1) : 0u;
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) {
+                        const uint32_t w = c < 32 ? w0 : w1;
+                        const bool vis = (d0 + c < geo.Pb) && ((w >> (c & 31)) & 1u);
+                        if (!vis) s[c] = -INFINITY;
+                    }
+                }
+                // ---- online softmax (log2 domain) ------------------------------
+                float mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 64; ++c) mx = fmaxf(mx, s[c]);
+                const float ms = mx * a.scale_log2;
+                const bool need = ms > m + kRescaleThreshold;
+                const float m_new = need ? ms : m;
+                if (__any_sync(0xffffffffu, need) && j > 0) {
+                    // O holds earlier chunks: wait for PV of the previous chunk, then rescale
+                    if (!warp_wait(&bar.pv_done, (gg - 1) & 1, abort, kWaitBudget)) { ok = false; break; }
+                    tc_fence_after();
+                    const float alpha = need ? fast_exp2(m - m_new) : 1.f;
+#pragma unroll
+                    for (int cb = 0; cb < D / 32; ++cb) {
+                        uint32_t o[32];
+                        tmem_ld32(tmem + lane_base + C::kOCol + cb * 32, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                        tmem_st32(tmem + lane_base + C::kOCol + cb * 32, o);
+                    }
+                    tmem_st_wait();
+                }
+                if (need) {
+                    l *= fast_exp2(m - m_new);             // 0 while m is -inf
+                    m = m_new;
+                }
+                const float base = (m == -INFINITY) ? 0.f : m;
+                unsigned char* ps = smem + C::kPOff + sb * C::kPBytes;
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    float p[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        p[e] = fast_exp2(fmaf(s[c8 * 8 + e], a.scale_log2, -base));
+                        l += p[e];
+                    }
+                    uint4 v;
+                    v.x = pack_bf16(p[0], p[1]);
+                    v.y = pack_bf16(p[2], p[3]);
+                    v.z = pack_bf16(p[4], p[5]);
+                    v.w = pack_bf16(p[6], p[7]);
+                    *reinterpret_cast<uint4*>(ps + sw128(t, c8)) = v;
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar.p_full[sb]);
+            }
+            if (!ok || !warp_wait(&bar.o_final, unit_iter & 1, abort, kWaitBudget)) { fail(); break; }
+            tc_fence_after();
+            // ---- epilogue ----------------------------------------------------------
+            const bool split_mode = !a.causal && geo.n_splits > 1;
+            if (!split_mode) {
+                const float inv = (valid && l > 0.f) ? 1.f / l : 0.f;
+                const bool write = valid || (!a.causal && qpos < a.P_max);
+                uint16_t* dst = nullptr;
+                if (write) {
+                    const size_t orow = a.causal ? (size_t)(geo.kv_base + qpos)
+                                                 : (size_t)geo.b * a.P_max + qpos;
+                    dst = a.o + (orow * a.Hq + hq0 + row % a.G) * D;
+                }
+#pragma unroll
+                for (int cb = 0; cb < D / 32; ++cb) {
+                    uint32_t o[32];
+                    tmem_ld32(tmem + lane_base + C::kOCol + cb * 32, o);
+                    tmem_ld_wait();
+                    if (write) {
+#pragma unroll
+                        for (int c = 0; c < 32; c += 8) {
+                            uint4 v;
+                            v.x = pack_bf16(__uint_as_float(o[c + 0]) * inv, __uint_as_float(o[c + 1]) * inv);
+                            v.y = pack_bf16(__uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv);
+                            v.z = pack_bf16(__uint_as_float(o[c + 4]) * inv, __uint_as_float(o[c + 5]) * inv);
+                            v.w = pack_bf16(__uint_as_float(o[c + 6]) * inv, __uint_as_float(o[c + 7]) * inv);
+                            *reinterpret_cast<uint4*>(dst + cb * 32 + c) = v;
+                        }
+                    }
+                }
+            } else {
+                // fp32 partials; the CTA that takes the last ticket of (b, h, tile) merges
+                const size_t unit_id = ((size_t)geo.b * a.Hkv + geo.h) * a.tiles + geo.tile;
+                const size_t prow = unit_id * kM + t;
+                float* op = a.o_part + (prow * a.splits + geo.split) * D;
+#pragma unroll
+                for (int cb = 0; cb < D / 32; ++cb) {
+                    uint32_t o[32];
+                    tmem_ld32(tmem + lane_base + C::kOCol + cb * 32, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4)
+                        *reinterpret_cast<float4*>(op + cb * 32 + c) =
+                            make_float4(__uint_as_float(o[c]), __uint_as_float(o[c + 1]),
+                                        __uint_as_float(o[c + 2]), __uint_as_float(o[c + 3]));
+                }
+                a.ml_part[prow * a.splits + geo.split] = make_float2(m, l);
+                __threadfence();
+                asm volatile("bar.sync 1, %0;" ::"r"(kSoftmaxThreads));
+                if (t == 0) {
+                    const unsigned tk = atomicAdd(a.tickets + unit_id, 1u);
+                    s_last = (tk == (unsigned)geo.n_splits - 1u);
+                }
+                asm volatile("bar.sync 1, %0;" ::"r"(kSoftmaxThreads));
+                if (s_last) {
+                    __threadfence();
+                    const int p = row / a.G;
+                    if (p < a.P_max) {
+                        float M = -INFINITY;
+                        for (int sp = 0; sp < geo.n_splits; ++sp)
+                            M = fmaxf(M, __ldcg(&a.ml_part[prow * a.splits + sp].x));
+                        float wsum[8];
+                        int nw = 0;
+                        float Ls = 0.f;
+                        (void)wsum; (void)nw;
+                        uint16_t* dst = a.o + (((size_t)geo.b * a.P_max + p) * a.Hq + hq0 + row % a.G) * D;
+                        for (int c = 0; c < D; c += 8) {
+                            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                            Ls = 0.f;
+                            if (valid && M != -INFINITY) {
+                                for (int sp = 0; sp < geo.n_splits; ++sp) {
+                                    const float2 ml = __ldcg(&a.ml_part[prow * a.splits + sp]);
+                                    if (ml.x == -INFINITY) continue;
+                                    const float w = exp2f(ml.x - M);
+                                    Ls += ml.y * w;
+                                    const float* src = a.o_part + (prow * a.splits + sp) * D + c;
+                                    const float4 x0 = __ldcg(reinterpret_cast<const float4*>(src));
+                                    const float4 x1 = __ldcg(reinterpret_cast<const float4*>(src + 4));
+                                    acc[0] += x0.x * w; acc[1] += x0.y * w; acc[2] += x0.z * w; acc[3] += x0.w * w;
+                                    acc[4] += x1.x * w; acc[5] += x1.y * w; acc[6] += x1.z * w; acc[7] += x1.w * w;
+                                }
+                            }
+                            const float inv = (valid && Ls > 0.f) ? 1.f / Ls : 0.f;
+                            uint4 v;
+                            v.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+                            v.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+                            v.z = pack_bf16(acc[4] * inv, acc[5] * inv);
+                            v.w = pack_bf16(acc[6] * inv, acc[7] * inv);
+                            *reinterpret_cast<uint4*>(dst + c) = v;
+                        }
+                    }
+                    if (t == 0) a.tickets[unit_id] = 0u;
+                }
+            }
+            g += n;
+            ++unit_iter;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, []() {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// [rows, heads, D] bf16 -> boxes of 64 positions x 1 head x 64 columns, 128-byte swizzle
+bool make_kv_map(CUtensorMap* map, const void* base, int64_t rows, int heads, int D)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    if (rows < 1) rows = 1;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)heads * D * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)kN};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int num_sms()
+{
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 148;
+    }
+    return n;
+}
+
+}  // namespace
+
+rd_attn_plan rd_attn_make_plan(bool causal, int B, int P_max, int Hq, int Hkv, int D,
+                               int max_kv)
+{
+    (void)D;
+    rd_attn_plan plan;
+    const int G = Hq / Hkv;
+    const long rows = causal ? (long)max_kv * G : (long)P_max * G;
+    plan.tiles = (int)((rows + kM - 1) / kM);
+    if (plan.tiles < 1) plan.tiles = 1;
+    const long ctx_chunks = causal ? 1 : ((long)max_kv + kN - 1) / kN;
+    const long base_units = (long)B * Hkv * plan.tiles;
+    const long target = 2L * 152;
+    long cps = ctx_chunks > 0 ? ctx_chunks : 1;           // context chunks per split
+    if (!causal && base_units < target && ctx_chunks > 4) {
+        long want = (target + base_units - 1) / base_units;
+        cps = (ctx_chunks + want - 1) / want;
+        if (cps < 4) cps = 4;                             // at least 256 positions per split
+    }
+    plan.split_len = (int)(cps * kN);
+    plan.splits = causal ? 1 : (int)((ctx_chunks + cps - 1) / cps);
+    if (plan.splits < 1) plan.splits = 1;
+    if (plan.splits > 1) {
+        const size_t unit_rows = (size_t)B * Hkv * plan.tiles * kM;
+        plan.ws_bytes = unit_rows * plan.splits * (size_t)D * sizeof(float) +
+                        unit_rows * plan.splits * sizeof(float2) +
+                        (size_t)B * Hkv * plan.tiles * sizeof(unsigned int);
+    } else {
+        plan.ws_bytes = 0;
+    }
+    return plan;
+}
+
+cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, int P_max,
+                                int Hq, int Hkv, int D, float scale, const void* q,
+                                const void* k_new, const void* v_new,
+                                const void* k_cache, const void* v_cache,
+                                const int64_t* ctx_offsets, int64_t total_kv, int max_kv,
+                                const int32_t* lens, const uint32_t* mask, int mask_words,
+                                void* o, void* workspace, int32_t* dev_status,
+                                cudaStream_t stream)
+{
+    TcArgs a;
+    a.causal = causal;
+    a.B = B;
+    a.P_max = P_max;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.G = Hq / Hkv;
+    a.tiles = plan.tiles;
+    a.splits = plan.splits;
+    a.chunks_per_split = plan.split_len / kN;
+    a.mask_words = mask_words;
+    a.n_units = B * Hkv * plan.tiles * plan.splits;
+    a.scale_log2 = scale * kLog2e;
+    a.q = static_cast<const uint16_t*>(q);
+    a.ctx_offsets = ctx_offsets;
+    a.total_kv = total_kv;
+    a.max_kv = max_kv;
+    a.lens = lens;
+    a.mask = mask;
+    a.o = static_cast<uint16_t*>(o);
+    a.status = dev_status;
+    a.o_part = nullptr;
+    a.ml_part = nullptr;
+    a.tickets = nullptr;
+    if (plan.splits > 1) {
+        const size_t unit_rows = (size_t)B * Hkv * plan.tiles * kM;
+        a.o_part = static_cast<float*>(workspace);
+        a.ml_part = reinterpret_cast<float2*>(a.o_part + unit_rows * plan.splits * D);
+        a.tickets = reinterpret_cast<unsigned int*>(a.ml_part + unit_rows * plan.splits);
+    }
+    CUtensorMap mkc, mvc, mkd, mvd;
+    const void* kc = causal ? k_new : k_cache;
+    const void* vc = causal ? v_new : v_cache;
+    const int64_t kc_rows = total_kv;
+    const int64_t kd_rows = causal ? total_kv : (int64_t)B * P_max;
+    const void* kd = causal ? k_new : k_new;
+    const void* vd = causal ? v_new : v_new;
+    if (kc == nullptr || kc_rows == 0) { kc = kd; vc = vd; }
+    if (!make_kv_map(&mkc, kc, kc_rows > 0 ? kc_rows : kd_rows, Hkv, D) ||
+        !make_kv_map(&mvc, vc, kc_rows > 0 ? kc_rows : kd_rows, Hkv, D) ||
+        !make_kv_map(&mkd, kd, kd_rows, Hkv, D) || !make_kv_map(&mvd, vd, kd_rows, Hkv, D))
+        return cudaErrorInvalidValue;
+    const int grid = (int)std::min<long>((long)a.n_units, (long)num_sms());
+    if (D == 128) {
+        using Cf = Cfg<128>;
+        cudaError_t e = cudaFuncSetAttribute(tree_attention_tc_kernel<128>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Cf::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        tree_attention_tc_kernel<128><<<grid, kThreads, Cf::kSmemBytes, stream>>>(a, mkc, mvc, mkd, mvd);
+    } else {
+        using Cf = Cfg<64>;
+        cudaError_t e = cudaFuncSetAttribute(tree_attention_tc_kernel<64>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Cf::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        tree_attention_tc_kernel<64><<<grid, kThreads, Cf::kSmemBytes, stream>>>(a, mkc, mvc, mkd, mvd);
+    }
+    return cudaGetLastError();
+}
