@@ -147,6 +147,61 @@ rd_status rd_tree_attention(int B, int P_max, int Hq, int Hkv, int D, float scal
                             int32_t* dev_status, rd_stream_t stream);
 
 /*
+ * rd_tree_attention_paged -- rd_tree_attention with the context in a paged KV
+ * cache (TensorRT-LLM's paged KV caching: NVIDIA blog "ReDrafter in
+ * TensorRT-LLM", introduction).  Same computation, outputs and workspace as
+ * rd_tree_attention (size the workspace with rd_tree_attention_workspace_size
+ * and the same max_ctx); only the context rows are found through a block table:
+ *
+ * k_pool,v_pool bf16 [num_pages, page_size, Hkv, D]
+ * block_table  int32 [B, max_pages]: context position j of request b is row
+ *              j % page_size of page block_table[b, j / page_size]
+ * ctx_lens     int32 [B] context lengths (<= max_ctx and <= max_pages*page_size,
+ *              else RD_DEV_BAD_LENGTH and the request is skipped)
+ * page_size    a multiple of 64 (RD_ERR_UNSUPPORTED otherwise); num_pages *
+ *              page_size < 2^31.  A page id outside [0, num_pages) sets
+ *              RD_DEV_BAD_INDEX (page 0 is read in its place).
+ */
+rd_status rd_tree_attention_paged(int B, int P_max, int Hq, int Hkv, int D, float scale,
+                                  const void* q, const void* k_new, const void* v_new,
+                                  const void* k_pool, const void* v_pool, int num_pages,
+                                  int page_size, const int32_t* block_table, int max_pages,
+                                  const int32_t* ctx_lens, int max_ctx,
+                                  const int32_t* packed_len, const uint32_t* mask,
+                                  int mask_words, void* o, void* workspace, size_t ws_bytes,
+                                  int32_t* dev_status, rd_stream_t stream);
+
+/*
+ * rd_commit_accepted -- append the K/V of each request's accepted path to its
+ * paged cache, after rd_greedy_accept.
+ *
+ * Source: NVIDIA blog "ReDrafter in TensorRT-LLM", introduction (verify the
+ * drafts and accept the best path before drafting the next tokens; paged KV
+ * caching).  The confirmed tokens of request b are the best beam's anchor and
+ * accepted drafts, nodes (w*, i) for i = 0..a with w* = best_beam[b] and
+ * a = n_accepted[b]; their rows k_new[b, unpacker[b, w*, i], :, :] (and v_new)
+ * are written at context position ctx_lens[b] + i (page
+ * block_table[b, pos / page_size], row pos % page_size), and
+ * new_ctx_lens[b] = ctx_lens[b] + a + 1.  The greedy token after the last
+ * accepted node has no K/V yet (it is the next step's anchor).
+ *
+ * k_new,v_new bf16 [B, P_max, Hkv, D]; unpacker int32 [B, W, L]; best_beam,
+ * n_accepted int32 [B]; k_pool,v_pool bf16 [num_pages, page_size, Hkv, D]
+ * (modified); block_table int32 [B, max_pages]; ctx_lens int32 [B] (read);
+ * new_ctx_lens int32 [B] (written; must not alias ctx_lens).
+ * A best beam, accepted length, unpacker index or page id out of range sets
+ * RD_DEV_BAD_INDEX; a position beyond max_pages*page_size sets
+ * RD_DEV_BAD_LENGTH; the offending row is skipped.
+ */
+rd_status rd_commit_accepted(int B, int W, int L, int P_max, int Hkv, int D,
+                             const void* k_new, const void* v_new, const int32_t* unpacker,
+                             const int32_t* best_beam, const int32_t* n_accepted,
+                             void* k_pool, void* v_pool, int num_pages, int page_size,
+                             const int32_t* block_table, int max_pages,
+                             const int32_t* ctx_lens, int32_t* new_ctx_lens,
+                             int32_t* dev_status, rd_stream_t stream);
+
+/*
  * rd_causal_attention -- causal prefill of the context-phase requests of an
  * in-flight batch (NVIDIA blog "ReDrafter in TensorRT-LLM", section
  * "Inflight-batching Compatible Engine": the batch splits into a context and a
@@ -180,6 +235,35 @@ rd_status rd_causal_attention(int B, int Hq, int Hkv, int D, float scale,
 rd_status rd_unpack(const void* packed, rd_dtype dt, int B, int P_max, int Dh,
                     const int32_t* unpacker, int W, int L, void* out,
                     int32_t* dev_status, rd_stream_t stream);
+
+/*
+ * rd_beam_search_step -- one step of the drafter's beam search (the step that
+ * produces the beams rd_pack_beams consumes).
+ *
+ * Source: Apple x NVIDIA news page, paragraph on the RNN draft model (from the
+ * initial token and the LLM's last hidden state the drafter runs a beam search
+ * that yields several candidate token sequences); "Recurrent Drafter for Fast
+ * Speculative Decoding in LLMs", abstract.  The drafter network itself is out
+ * of scope: its logits are an input.
+ *
+ * Candidate (w, v) of request b scores
+ *   scores_in[b, w] + logits[b, w, v] - log sum_u exp(logits[b, w, u]);
+ * a beam whose score is -inf (not live yet) has no candidates.  The W best
+ * candidates, best first (equal scores: the lower flat index w*V + v first),
+ * become the new beams: beams_out[b, r] = beams_in[b, parent[b, r]] followed
+ * by token v_r, scores_out[b, r] = its score.  Scores are computed in fp32;
+ * candidates whose scores differ by less than their fp32 rounding may be
+ * ordered either way.
+ *
+ * logits bf16 [B, W, V]; scores_in fp32 [B, W]; beams_in int32 [B, W, t]
+ * (t >= 0; may be NULL when t == 0); beams_out int32 [B, W, t+1];
+ * scores_out fp32 [B, W]; parent int32 [B, W].  1 <= W <= 16, V >= W.
+ * Fewer than W live candidates set RD_DEV_BAD_LENGTH (parent -1, token -1).
+ */
+rd_status rd_beam_search_step(const void* logits, const float* scores_in,
+                              const int32_t* beams_in, int B, int W, int V, int t,
+                              int32_t* beams_out, float* scores_out, int32_t* parent,
+                              int32_t* dev_status, rd_stream_t stream);
 
 /*
  * rd_greedy_accept -- greedy verification of the drafts.

@@ -52,9 +52,13 @@ def _load():
                                                   P, P, P, P, I, P, I]
             lib.oracle_causal_attention.argtypes = [I, I, I, I, ctypes.c_double, P, P, P, P,
                                                     P, I]
+            lib.oracle_tree_attention_paged.argtypes = [I, I, I, I, I, ctypes.c_double, P, P, P,
+                                                        P, P, I, I, P, I, P, P, P, I, P, I]
             lib.oracle_greedy_accept.argtypes = [P, I, I, I, P, P, P, I, I, P, P, P, P, P]
+            lib.oracle_beam_search_step.argtypes = [P, P, P, I, I, I, I, P, P, P]
             for f in (lib.oracle_pack, lib.oracle_tree_attention,
-                      lib.oracle_causal_attention, lib.oracle_greedy_accept):
+                      lib.oracle_tree_attention_paged, lib.oracle_causal_attention,
+                      lib.oracle_greedy_accept, lib.oracle_beam_search_step):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -115,6 +119,56 @@ def oracle_tree_attention(q, k_new, v_new, k_cache, v_cache, ctx_offsets, packed
     return o
 
 
+def oracle_tree_attention_paged(q, k_new, v_new, k_pool, v_pool, block_table, ctx_lens,
+                                packed_len, mask, scale: float = 0.0,
+                                n_threads: int | None = None) -> np.ndarray:
+    """Tree-masked attention with the context in a paged cache (see
+    oracle_tree_attention_paged in rd_oracle.c): k_pool/v_pool [pages, page_size,
+    Hkv, D] (uint16 bf16 bits), block_table int32 [B, max_pages], ctx_lens int32 [B]."""
+    q = _c(q, np.uint16); k_new = _c(k_new, np.uint16); v_new = _c(v_new, np.uint16)
+    k_pool = _c(k_pool, np.uint16); v_pool = _c(v_pool, np.uint16)
+    block_table = _c(block_table, np.int32); ctx_lens = _c(ctx_lens, np.int32)
+    packed_len = _c(packed_len, np.int32); mask = _c(mask, np.uint32)
+    B, P, Hq, D = q.shape
+    Hkv = k_new.shape[2]
+    num_pages, page_size = k_pool.shape[0], k_pool.shape[1]
+    o = np.zeros((B, P, Hq, D), np.float64)
+    rc = _load().oracle_tree_attention_paged(
+        B, P, Hq, Hkv, D, float(scale), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool),
+        _ptr(v_pool), num_pages, page_size, _ptr(block_table), block_table.shape[1],
+        _ptr(ctx_lens), _ptr(packed_len), _ptr(mask), mask.shape[2], _ptr(o),
+        n_threads or n_threads_default())
+    if rc != 0:
+        raise ValueError(f"oracle_tree_attention_paged rejected the input (rc={rc})")
+    return o
+
+
+def oracle_commit_accepted(k_new, v_new, unpacker, best_beam, n_accepted, k_pool, v_pool,
+                           block_table, ctx_lens):
+    """Append the K/V of each request's accepted path to its paged cache.
+
+    The accepted path of request b is its best beam's anchor and accepted drafts,
+    nodes (w*, 0..a) with a = n_accepted[b]; their K/V rows k_new[b, unpacker[b, w*, i]]
+    go to context positions ctx_lens[b] + i of the paged cache (the tokens the
+    verification step has confirmed; NVIDIA blog introduction: accept the best
+    path before drafting the next tokens).  Returns (k_pool, v_pool, new_ctx_lens)
+    as new arrays; the inputs are not modified."""
+    k_pool = np.array(k_pool, copy=True)
+    v_pool = np.array(v_pool, copy=True)
+    new_lens = np.array(ctx_lens, dtype=np.int32, copy=True)
+    page_size = k_pool.shape[1]
+    for b in range(unpacker.shape[0]):
+        w, a, C = int(best_beam[b]), int(n_accepted[b]), int(ctx_lens[b])
+        for i in range(a + 1):
+            pos = C + i
+            page = int(block_table[b, pos // page_size])
+            node = int(unpacker[b, w, i])
+            k_pool[page, pos % page_size] = k_new[b, node]
+            v_pool[page, pos % page_size] = v_new[b, node]
+        new_lens[b] = C + a + 1
+    return k_pool, v_pool, new_lens
+
+
 def oracle_causal_attention(q, k, v, cu_seqlens, scale: float = 0.0,
                             n_threads: int | None = None) -> np.ndarray:
     """Causal attention per sequence in fp64: q [T,Hq,D], k/v [T,Hkv,D] (uint16 bf16 bits),
@@ -147,6 +201,25 @@ def oracle_greedy_accept(logits, beams, unpacker, packed_len) -> dict:
                                       _ptr(out["n_accepted"]), _ptr(out["out_tokens"]))
     if rc != 0:
         raise ValueError(f"oracle_greedy_accept rejected the input (rc={rc})")
+    return out
+
+
+def oracle_beam_search_step(logits, scores_in, beams_in) -> dict:
+    """One beam-search step in fp64: logits [B, W, V] (uint16 bf16 bits),
+    scores_in [B, W] (cumulative log-probabilities; -inf = beam not live),
+    beams_in int32 [B, W, t].  Returns beams [B, W, t+1], scores [B, W], parent [B, W]."""
+    logits = _c(logits, np.uint16)
+    scores_in = _c(scores_in, np.float64)
+    beams_in = _c(beams_in, np.int32)
+    B, W, V = logits.shape
+    t = beams_in.shape[2]
+    out = dict(beams=np.zeros((B, W, t + 1), np.int32), scores=np.zeros((B, W), np.float64),
+               parent=np.zeros((B, W), np.int32))
+    rc = _load().oracle_beam_search_step(_ptr(logits), _ptr(scores_in), _ptr(beams_in), B, W, V,
+                                         t, _ptr(out["beams"]), _ptr(out["scores"]),
+                                         _ptr(out["parent"]))
+    if rc != 0:
+        raise ValueError(f"oracle_beam_search_step rejected the input (rc={rc})")
     return out
 
 

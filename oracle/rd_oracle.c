@@ -20,8 +20,16 @@
  *                          page, SpecInfer "Token Tree Verifier": one kernel with
  *                          a topology-aware causal mask replaces per-sequence
  *                          attention).
+ *   oracle_tree_attention_paged  the same attention with the context read
+ *                          through a paged KV cache (NVIDIA blog, introduction:
+ *                          TensorRT-LLM's paged KV caching): position j of
+ *                          request b lives in page block_table[b][j / page_size],
+ *                          row j % page_size.
  *   oracle_causal_attention  causal prefill of context-phase requests (NVIDIA
  *                          blog, "Inflight-batching Compatible Engine").
+ *   oracle_beam_search_step  one step of the drafter's beam search (news page,
+ *                          paragraph on the RNN draft model): the W best
+ *                          (beam, token) candidates by cumulative log-probability.
  *   oracle_greedy_accept   greedy verification: argmax per packed position,
  *                          longest accepted draft prefix per beam, best beam
  *                          (NVIDIA blog introduction: verify and accept the best
@@ -152,14 +160,35 @@ typedef struct {
     int next_task, n_tasks;
     pthread_mutex_t lock;
     int err;
+    /* paged context (ctx_lens != NULL): rows of k_cache/v_cache are pool rows */
+    const int32_t* ctx_lens;
+    const int32_t* block_table;
+    int max_pages, page_size;
 } tree_job;
+
+/* context length of request b */
+static int64_t ctx_len(const tree_job* J, int b)
+{
+    if (J->ctx_lens) return J->ctx_lens[b];
+    return J->ctx_offsets[b + 1] - J->ctx_offsets[b];
+}
+
+/* cache row holding context position j of request b */
+static int64_t ctx_row(const tree_job* J, int b, int64_t j)
+{
+    if (J->ctx_lens) {
+        int64_t page = J->block_table[(size_t)b * J->max_pages + j / J->page_size];
+        return page * J->page_size + j % J->page_size;
+    }
+    return J->ctx_offsets[b] + j;
+}
 
 static void tree_task(tree_job* J, int task, const uint16_t** keys, const uint16_t** vals,
                       double* s_buf)
 {
     int b = task / J->Hq, hq = task % J->Hq;
     int G = J->Hq / J->Hkv, h = hq / G;
-    int64_t c0 = J->ctx_offsets[b], C = J->ctx_offsets[b + 1] - c0;
+    int64_t C = ctx_len(J, b);
     int Pb = J->packed_len[b];
     size_t qrow = (size_t)J->Hq * J->D, kvrow = (size_t)J->Hkv * J->D;
     for (int p = 0; p < J->P_max; ++p) {
@@ -170,8 +199,9 @@ static void tree_task(tree_job* J, int task, const uint16_t** keys, const uint16
         }
         int n = 0;
         for (int64_t j = 0; j < C; ++j) {     /* every context key is visible */
-            keys[n] = J->k_cache + (size_t)(c0 + j) * kvrow + (size_t)h * J->D;
-            vals[n] = J->v_cache + (size_t)(c0 + j) * kvrow + (size_t)h * J->D;
+            int64_t r = ctx_row(J, b, j);
+            keys[n] = J->k_cache + (size_t)r * kvrow + (size_t)h * J->D;
+            vals[n] = J->v_cache + (size_t)r * kvrow + (size_t)h * J->D;
             ++n;
         }
         const uint32_t* row = J->mask + ((size_t)b * J->P_max + p) * J->NW;
@@ -192,7 +222,7 @@ static void* tree_worker(void* arg)
     tree_job* J = (tree_job*)arg;
     int64_t max_ctx = 0;
     for (int b = 0; b < J->B; ++b) {
-        int64_t c = J->ctx_offsets[b + 1] - J->ctx_offsets[b];
+        int64_t c = ctx_len(J, b);
         if (c > max_ctx) max_ctx = c;
     }
     size_t cap = (size_t)max_ctx + (size_t)J->P_max;
@@ -216,6 +246,16 @@ static void* tree_worker(void* arg)
     return NULL;
 }
 
+static int run_tree_job(tree_job* J, int n_threads)
+{
+    if (n_threads < 1) n_threads = 1;
+    if (n_threads > 256) n_threads = 256;
+    pthread_t th[256];
+    for (int t = 0; t < n_threads; ++t) pthread_create(&th[t], NULL, tree_worker, J);
+    for (int t = 0; t < n_threads; ++t) pthread_join(th[t], NULL);
+    return J->err;
+}
+
 int oracle_tree_attention(int B, int P_max, int Hq, int Hkv, int D, double scale,
                           const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
                           const uint16_t* k_cache, const uint16_t* v_cache,
@@ -228,13 +268,34 @@ int oracle_tree_attention(int B, int P_max, int Hq, int Hkv, int D, double scale
             ctx_offsets[b + 1] < ctx_offsets[b]) return -1;
     tree_job J = {B, P_max, Hq, Hkv, D, mask_words, scale > 0 ? scale : 1.0 / sqrt((double)D),
                   q, k_new, v_new, k_cache, v_cache, ctx_offsets, packed_len, mask, o,
-                  0, B * Hq, PTHREAD_MUTEX_INITIALIZER, 0};
-    if (n_threads < 1) n_threads = 1;
-    pthread_t th[256];
-    if (n_threads > 256) n_threads = 256;
-    for (int t = 0; t < n_threads; ++t) pthread_create(&th[t], NULL, tree_worker, &J);
-    for (int t = 0; t < n_threads; ++t) pthread_join(th[t], NULL);
-    return J.err;
+                  0, B * Hq, PTHREAD_MUTEX_INITIALIZER, 0, NULL, NULL, 0, 1};
+    return run_tree_job(&J, n_threads);
+}
+
+int oracle_tree_attention_paged(int B, int P_max, int Hq, int Hkv, int D, double scale,
+                                const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                                const uint16_t* k_pool, const uint16_t* v_pool, int num_pages,
+                                int page_size, const int32_t* block_table, int max_pages,
+                                const int32_t* ctx_lens, const int32_t* packed_len,
+                                const uint32_t* mask, int mask_words, double* o, int n_threads)
+{
+    if (B < 0 || P_max <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 || page_size <= 0 ||
+        max_pages < 0)
+        return -1;
+    for (int b = 0; b < B; ++b) {
+        if (packed_len[b] < 0 || packed_len[b] > P_max || ctx_lens[b] < 0 ||
+            (int64_t)ctx_lens[b] > (int64_t)max_pages * page_size)
+            return -1;
+        for (int64_t p = 0; p < ((int64_t)ctx_lens[b] + page_size - 1) / page_size; ++p) {
+            int32_t pg = block_table[(size_t)b * max_pages + p];
+            if (pg < 0 || pg >= num_pages) return -1;
+        }
+    }
+    tree_job J = {B, P_max, Hq, Hkv, D, mask_words, scale > 0 ? scale : 1.0 / sqrt((double)D),
+                  q, k_new, v_new, k_pool, v_pool, NULL, packed_len, mask, o,
+                  0, B * Hq, PTHREAD_MUTEX_INITIALIZER, 0, ctx_lens, block_table, max_pages,
+                  page_size};
+    return run_tree_job(&J, n_threads);
 }
 
 typedef struct {
@@ -358,5 +419,59 @@ int oracle_greedy_accept(const uint16_t* logits, int B, int P_max, int V,
         if (last < 0 || last >= Pb) return -4;
         ot[best_a] = g[last];
     }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* drafter beam search                                                       */
+/* ------------------------------------------------------------------------ */
+/* One step of the drafter's beam search (Apple x NVIDIA news page, paragraph
+ * on the RNN draft model: from the initial token and the LLM's last hidden
+ * state the drafter runs a beam search that yields several candidate token
+ * sequences).  Candidate (w, v) scores scores_in[w] + log softmax(logits[w])[v];
+ * a beam with score -inf has no candidates.  The W best candidates, best first
+ * (equal scores: lower w*V + v first), become the new beams. */
+int oracle_beam_search_step(const uint16_t* logits, const double* scores_in,
+                            const int32_t* beams_in, int B, int W, int V, int t,
+                            int32_t* beams_out, double* scores_out, int32_t* parent)
+{
+    if (B < 0 || W <= 0 || V < W || t < 0) return -1;
+    double* cand = malloc(sizeof(double) * (size_t)W * V);
+    unsigned char* taken = malloc((size_t)W * V);
+    if (!cand || !taken) { free(cand); free(taken); return -3; }
+    for (int b = 0; b < B; ++b) {
+        const uint16_t* lg = logits + (size_t)b * W * V;
+        for (int w = 0; w < W; ++w) {
+            const uint16_t* row = lg + (size_t)w * V;
+            double mx = -INFINITY, sum = 0.0;
+            for (int v = 0; v < V; ++v) {
+                double x = bf16_to_f64(row[v]);
+                if (x > mx) mx = x;
+            }
+            for (int v = 0; v < V; ++v) sum += exp(bf16_to_f64(row[v]) - mx);
+            double lse = mx + log(sum);
+            double s = scores_in[(size_t)b * W + w];
+            for (int v = 0; v < V; ++v)
+                cand[(size_t)w * V + v] = (s == -INFINITY) ? -INFINITY : s + bf16_to_f64(row[v]) - lse;
+        }
+        memset(taken, 0, (size_t)W * V);
+        for (int r = 0; r < W; ++r) {
+            int best = -1;
+            for (int i = 0; i < W * V; ++i) {
+                if (taken[i] || cand[i] == -INFINITY) continue;
+                if (best < 0 || cand[i] > cand[best]) best = i;   /* first maximum: lower index */
+            }
+            if (best < 0) { free(cand); free(taken); return -4; }
+            taken[best] = 1;
+            int pw = best / V, tok = best % V;
+            parent[(size_t)b * W + r] = pw;
+            scores_out[(size_t)b * W + r] = cand[best];
+            for (int j = 0; j < t; ++j)
+                beams_out[((size_t)b * W + r) * (t + 1) + j] = beams_in[((size_t)b * W + pw) * t + j];
+            beams_out[((size_t)b * W + r) * (t + 1) + t] = tok;
+        }
+    }
+    free(cand);
+    free(taken);
     return 0;
 }

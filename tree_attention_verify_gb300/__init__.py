@@ -21,7 +21,8 @@ from . import _build
 __all__ = [
     "rd_pack_beams", "rd_tree_attention", "rd_tree_attention_workspace_size",
     "rd_causal_attention", "rd_unpack", "rd_greedy_accept",
-    "rd_greedy_accept_workspace_size", "rd_greedy_accept_noalloc", "RdError", "DEV_BAD_INDEX", "DEV_BAD_TOKEN",
+    "rd_greedy_accept_workspace_size", "rd_greedy_accept_noalloc",
+    "rd_tree_attention_paged", "rd_commit_accepted", "rd_beam_search_step", "RdError", "DEV_BAD_INDEX", "DEV_BAD_TOKEN",
     "DEV_OVERFLOW", "DEV_BAD_LENGTH", "DEV_TIMEOUT", "lib_path",
 ]
 
@@ -55,6 +56,10 @@ def _load() -> ctypes.CDLL:
         "rd_greedy_accept_workspace_size": [I, I, I],
         "rd_greedy_accept": [P, I, I, I, P, P, P, I, I, P, P, P, P, P, P, S, P, P],
         "rd_greedy_accept_noalloc": [P, I, I, I, P, P, P, I, I, P, P, P, P, P, P, P],
+        "rd_tree_attention_paged": [I, I, I, I, I, F, P, P, P, P, P, I, I, P, I, P, I, P, P, I,
+                                    P, P, S, P, P],
+        "rd_commit_accepted": [I, I, I, I, I, I, P, P, P, P, P, P, P, I, I, P, I, P, P, P, P],
+        "rd_beam_search_step": [P, P, P, I, I, I, I, P, P, P, P, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -176,6 +181,67 @@ def rd_tree_attention(q, k_new, v_new, k_cache, v_cache, ctx_offsets, packed_len
     return out
 
 
+def rd_tree_attention_paged(q, k_new, v_new, k_pool, v_pool, block_table, ctx_lens, packed_len,
+                            mask, *, max_ctx: int, scale: float = 0.0, out=None, workspace=None,
+                            dev_status=None, stream=None) -> torch.Tensor:
+    """rd_tree_attention with the context in a paged cache: k_pool/v_pool
+    [num_pages, page_size, Hkv, D] bf16, block_table int32 [B, max_pages],
+    ctx_lens int32 [B] (see rd_tree_attention_paged in rd.h)."""
+    for n, t in (("q", q), ("k_new", k_new), ("v_new", v_new)):
+        _need(t, n, torch.bfloat16, ndim=4)
+    _need(k_pool, "k_pool", torch.bfloat16, ndim=4)
+    _need(v_pool, "v_pool", torch.bfloat16, ndim=4)
+    _need(block_table, "block_table", torch.int32, ndim=2)
+    _need(ctx_lens, "ctx_lens", torch.int32, ndim=1)
+    _need(packed_len, "packed_len", torch.int32, ndim=1)
+    if mask.dim() != 3 or not mask.is_contiguous() or mask.element_size() != 4:
+        raise ValueError("mask must be a contiguous 32-bit [B, P_max, NW] tensor")
+    B, P, Hq, D = q.shape
+    Hkv = k_new.shape[2]
+    n_pages, page_size = k_pool.shape[0], k_pool.shape[1]
+    if k_pool.shape[2:] != (Hkv, D) or v_pool.shape != k_pool.shape:
+        raise ValueError("k_pool/v_pool must be [num_pages, page_size, Hkv, D]")
+    if block_table.shape[0] != B or ctx_lens.numel() != B or packed_len.numel() != B:
+        raise ValueError("block_table/ctx_lens/packed_len do not match the batch")
+    if out is None:
+        out = torch.empty_like(q)
+    ws_need = rd_tree_attention_workspace_size(B, P, Hq, Hkv, D, max_ctx)
+    if ws_need and workspace is None:
+        workspace = torch.zeros(ws_need, dtype=torch.uint8, device=q.device)
+    _check("rd_tree_attention_paged", _lib.rd_tree_attention_paged(
+        B, P, Hq, Hkv, D, float(scale), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool),
+        _ptr(v_pool), n_pages, page_size, _ptr(block_table), block_table.shape[1],
+        _ptr(ctx_lens), int(max_ctx), _ptr(packed_len), _ptr(mask), int(mask.shape[2]),
+        _ptr(out), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(),
+        _ptr(dev_status), _stream(stream)))
+    return out
+
+
+def rd_commit_accepted(k_new, v_new, unpacker, best_beam, n_accepted, k_pool, v_pool,
+                       block_table, ctx_lens, *, new_ctx_lens=None, dev_status=None,
+                       stream=None) -> torch.Tensor:
+    """Append the accepted path's K/V to the paged cache (k_pool/v_pool modified in
+    place).  Returns new_ctx_lens = ctx_lens + n_accepted + 1 (see rd.h)."""
+    _need(k_new, "k_new", torch.bfloat16, ndim=4)
+    _need(v_new, "v_new", torch.bfloat16, ndim=4)
+    _need(k_pool, "k_pool", torch.bfloat16, ndim=4)
+    _need(v_pool, "v_pool", torch.bfloat16, ndim=4)
+    for n, t in (("unpacker", unpacker), ("best_beam", best_beam), ("n_accepted", n_accepted),
+                 ("block_table", block_table), ("ctx_lens", ctx_lens)):
+        _need(t, n, torch.int32)
+    B, P, Hkv, D = k_new.shape
+    _, W, L = unpacker.shape
+    if new_ctx_lens is None:
+        new_ctx_lens = torch.empty_like(ctx_lens)
+    _check("rd_commit_accepted", _lib.rd_commit_accepted(
+        B, W, L, P, Hkv, D, _ptr(k_new), _ptr(v_new), _ptr(unpacker), _ptr(best_beam),
+        _ptr(n_accepted), _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], k_pool.shape[1],
+        _ptr(block_table), block_table.shape[1], _ptr(ctx_lens), _ptr(new_ctx_lens),
+        _ptr(dev_status), _stream(stream)))
+    return new_ctx_lens
+
+
 def rd_causal_attention(q, k, v, cu_seqlens, *, max_seqlen: int, scale: float = 0.0,
                         out=None, dev_status=None, stream=None) -> torch.Tensor:
     """Causal prefill attention: q [T,Hq,D], k/v [T,Hkv,D] bf16, cu_seqlens int32 [B+1]."""
@@ -267,4 +333,25 @@ def rd_greedy_accept_noalloc(logits, beams, unpacker, packed_len, *, out=None, d
         _ptr(logits), B, P, V, _ptr(beams), _ptr(unpacker), _ptr(packed_len), W, L,
         _ptr(out["argmax"]), _ptr(out["accept_len"]), _ptr(out["best_beam"]),
         _ptr(out["n_accepted"]), _ptr(out["out_tokens"]), _ptr(dev_status), _stream(stream)))
+    return out
+
+
+def rd_beam_search_step(logits, scores_in, beams_in, *, out=None, dev_status=None,
+                        stream=None) -> dict:
+    """One beam-search step of the drafter (see rd_beam_search_step in rd.h):
+    logits bf16 [B, W, V], scores_in fp32 [B, W], beams_in int32 [B, W, t].
+    Returns dict(beams [B, W, t+1], scores [B, W], parent [B, W])."""
+    _need(logits, "logits", torch.bfloat16, ndim=3)
+    _need(scores_in, "scores_in", torch.float32, ndim=2)
+    _need(beams_in, "beams_in", torch.int32, ndim=3)
+    B, W, V = logits.shape
+    t = beams_in.shape[2]
+    if out is None:
+        out = dict(beams=_empty((B, W, t + 1), torch.int32, logits),
+                   scores=_empty((B, W), torch.float32, logits),
+                   parent=_empty((B, W), torch.int32, logits))
+    _check("rd_beam_search_step", _lib.rd_beam_search_step(
+        _ptr(logits), _ptr(scores_in), _ptr(beams_in) if t > 0 else None, B, W, V, t,
+        _ptr(out["beams"]), _ptr(out["scores"]), _ptr(out["parent"]), _ptr(dev_status),
+        _stream(stream)))
     return out

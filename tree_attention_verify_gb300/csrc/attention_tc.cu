@@ -59,7 +59,7 @@ template <int D> struct Cfg {
     static constexpr int kPOff = kQOff + kQBytes;
     static constexpr int kStageOff = kPOff + 2 * kPBytes;
     static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
-    static constexpr int kSmemBytes = kBarOff + 256 + 1024;   // + barriers + alignment slack
+    static constexpr int kSmemBytes = kBarOff + 512 + 1024;   // + barriers + alignment slack
     static constexpr uint32_t kTmemCols = 256;          // S: 2 x 64, O: D (<= 128)
     static constexpr uint32_t kSCol = 0;
     static constexpr uint32_t kOCol = 128;
@@ -80,6 +80,11 @@ struct TcArgs {
     float2* ml_part;
     unsigned int* tickets;
     int32_t* status;
+    // paged context (block_table != nullptr): position j of request b is row
+    // j % page_size of page block_table[b * max_pages + j / page_size]
+    const int32_t* block_table;
+    const int32_t* ctx_lens;
+    int max_pages, page_size, num_pages;
 };
 
 struct Barriers {
@@ -141,12 +146,20 @@ __device__ __forceinline__ UnitGeo unit_geo(const TcArgs& a, int u)
             g.live = true;
         }
     } else {
-        const int64_t c0 = a.ctx_offsets[g.b], c1 = a.ctx_offsets[g.b + 1];
-        g.kv_base = c0;
-        g.C = (int)(c1 - c0);
         g.Pb = a.lens[g.b];
-        bad = c0 < 0 || c1 < c0 || c1 - c0 > a.max_kv || c1 > a.total_kv || g.Pb < 0 ||
-              g.Pb > a.P_max;
+        if (a.block_table != nullptr) {
+            const int c = a.ctx_lens[g.b];
+            g.kv_base = 0;
+            g.C = c;
+            bad = c < 0 || c > a.max_kv || (long long)c > (long long)a.max_pages * a.page_size ||
+                  g.Pb < 0 || g.Pb > a.P_max;
+        } else {
+            const int64_t c0 = a.ctx_offsets[g.b], c1 = a.ctx_offsets[g.b + 1];
+            g.kv_base = c0;
+            g.C = (int)(c1 - c0);
+            bad = c0 < 0 || c1 < c0 || c1 - c0 > a.max_kv || c1 > a.total_kv || g.Pb < 0 ||
+                  g.Pb > a.P_max;
+        }
         if (bad) { g.C = 0; g.Pb = 0; }
         g.n_rows = g.Pb * a.G;
         const int row0 = g.tile * kM;
@@ -256,8 +269,23 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 const UnitGeo geo = unit_geo(a, u);
                 if (!geo.live) continue;
                 const int n = geo.n_ctx + geo.n_draft;
+                // first cache row of context chunk j (paged: looked up one chunk ahead,
+                // so the block-table read overlaps the wait for a free stage)
+                auto page_row = [&](int j) -> int {
+                    const int pos0 = (geo.c_first + j) * kN;
+                    int pg = __ldg(a.block_table + (size_t)geo.b * a.max_pages + pos0 / a.page_size);
+                    if (pg < 0 || pg >= a.num_pages) {
+                        rd_flag(a.status, RD_DEV_BAD_INDEX);
+                        pg = 0;
+                    }
+                    return pg * a.page_size + pos0 % a.page_size;
+                };
+                const bool paged = a.block_table != nullptr;
+                int next_row = (paged && geo.n_ctx > 0) ? page_row(0) : 0;
                 for (int j = 0; j < n; ++j, ++g) {
                     const int st = g % C::kStages;
+                    const int this_row = next_row;
+                    if (paged && j + 1 < geo.n_ctx) next_row = page_row(j + 1);
                     if (g >= (uint32_t)C::kStages &&
                         !mbar_wait(&bar.kv_empty[st], ((g / C::kStages) - 1) & 1, abort,
                                    kWaitBudget)) { fail(); break; }
@@ -269,7 +297,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                     int z;
                     if (j < geo.n_ctx) {
                         mk = &map_kc; mv = &map_vc;
-                        z = (int)(geo.kv_base + (int64_t)(geo.c_first + j) * kN);
+                        z = paged ? this_row : (int)(geo.kv_base + (int64_t)(geo.c_first + j) * kN);
                     } else {
                         mk = &map_kd; mv = &map_vd;
                         z = geo.b * a.P_max + (j - geo.n_ctx) * kN;
@@ -291,24 +319,37 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16(kM, kN, false, false);
             constexpr uint32_t idPV = idesc_bf16(kM, D, false, true);
-            const uint32_t q_base = smem_addr(smem + C::kQOff);
             uint32_t g = 0, unit_iter = 0;
-            auto issue_pv = [&](uint32_t gp, int jp) -> bool {
-                const int sb = gp & 1;
-                if (!mbar_wait(&bar.p_full[sb], (gp >> 1) & 1, abort, kWaitBudget)) return false;
-                tc_fence_after();
-                const uint32_t p_base = smem_addr(smem + C::kPOff + sb * C::kPBytes);
-                const uint32_t v_base =
-                    smem_addr(smem + C::kStageOff + (gp % C::kStages) * C::kStageBytes + C::kKBytes);
+            // Shared-memory descriptors differ only in their start-address field
+            // (bits 0-13, address >> 4): build each base once and add offsets,
+            // which keeps the issuing thread's work per MMA to two additions.
+            const uint64_t q_desc = smem_desc(smem_addr(smem + C::kQOff), 16, 1024, kSwizzle128B);
+            const uint64_t k_desc = smem_desc(smem_addr(smem + C::kStageOff), 16, 1024, kSwizzle128B);
+            const uint64_t v_desc = smem_desc(smem_addr(smem + C::kStageOff + C::kKBytes), kN * 128,
+                                              1024, kSwizzle128B);
+            const uint64_t p_desc = smem_desc(smem_addr(smem + C::kPOff), 16, 1024, kSwizzle128B);
+            // S = Q K^T for chunk gs (D/16 K-steps) into TMEM tile gs & 1.
+            auto issue_s = [&](uint32_t gs) {
+                const uint64_t kd = k_desc + (uint64_t)(((gs % C::kStages) * C::kStageBytes) >> 4);
+                const uint32_t d_tmem = tmem + C::kSCol + (gs & 1) * kN;
 #pragma unroll
-                for (int kk = 0; kk < kN / 16; ++kk) {
-                    const uint64_t ad = smem_desc(p_base + kk * 32, 16, 1024, kSwizzle128B);
-                    const uint64_t bd = smem_desc(v_base + kk * 2048, kN * 128, 1024, kSwizzle128B);
-                    mma_bf16(tmem + C::kOCol, ad, bd, idPV, jp > 0 || kk > 0);
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = ((ks >> 2) * (kN * 128) + (ks & 3) * 32) >> 4;
+                    const uint32_t qoff = ((ks >> 2) * (kM * 128) + (ks & 3) * 32) >> 4;
+                    mma_bf16(d_tmem, q_desc + qoff, kd + off, idS, ks > 0);
                 }
+                mma_commit(&bar.s_full[gs & 1]);
+            };
+            // O += P V for chunk gp (4 K-steps of 16 positions).
+            auto issue_pv = [&](uint32_t gp, bool first) {
+                const uint64_t vd = v_desc + (uint64_t)(((gp % C::kStages) * C::kStageBytes) >> 4);
+                const uint64_t pd = p_desc + (uint64_t)(((gp & 1) * C::kPBytes) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < kN / 16; ++kk)
+                    mma_bf16(tmem + C::kOCol, pd + (uint64_t)((kk * 32) >> 4),
+                             vd + (uint64_t)((kk * 2048) >> 4), idPV, !(first && kk == 0));
                 mma_commit(&bar.kv_empty[gp % C::kStages]);
                 mma_commit(&bar.pv_done);
-                return true;
             };
             for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
                 const UnitGeo geo = unit_geo(a, u);
@@ -317,26 +358,34 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 if (!mbar_wait(&bar.q_full, unit_iter & 1, abort, kWaitBudget)) { fail(); break; }
                 tc_fence_after();
                 bool ok = true;
+                // S_j as soon as chunk j has landed and its TMEM tile is free, then
+                // PV_{j-1} once the softmax has written P_{j-1}.
                 for (int j = 0; j < n && ok; ++j) {
                     const uint32_t gg = g + j;
-                    const int st = gg % C::kStages;
-                    const int sb = gg & 1;
-                    if (!mbar_wait(&bar.kv_full[st], (gg / C::kStages) & 1, abort, kWaitBudget)) { ok = false; break; }
-                    if (gg >= 2 && !mbar_wait(&bar.s_free[sb], ((gg >> 1) - 1) & 1, abort, kWaitBudget)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t k_base = smem_addr(smem + C::kStageOff + st * C::kStageBytes);
-#pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint32_t koff = (ks >> 2) * (kN * 128) + (ks & 3) * 32;
-                        const uint32_t qoff = (ks >> 2) * (kM * 128) + (ks & 3) * 32;
-                        const uint64_t ad = smem_desc(q_base + qoff, 16, 1024, kSwizzle128B);
-                        const uint64_t bd = smem_desc(k_base + koff, 16, 1024, kSwizzle128B);
-                        mma_bf16(tmem + C::kSCol + sb * kN, ad, bd, idS, ks > 0);
+                    if (!mbar_wait(&bar.kv_full[gg % C::kStages], (gg / C::kStages) & 1, abort, kWaitBudget) ||
+                        (gg >= 2 && !mbar_wait(&bar.s_free[gg & 1], ((gg >> 1) - 1) & 1, abort, kWaitBudget))) {
+                        ok = false;
+                        break;
                     }
-                    mma_commit(&bar.s_full[sb]);
-                    if (j >= 1 && !issue_pv(gg - 1, j - 1)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_s(gg);
+                    if (j >= 1) {
+                        if (!mbar_wait(&bar.p_full[(gg - 1) & 1], ((gg - 1) >> 1) & 1, abort, kWaitBudget)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_pv(gg - 1, j == 1);
+                    }
                 }
-                if (ok && !issue_pv(g + n - 1, n - 1)) ok = false;
+                if (ok) {
+                    const uint32_t gl = g + n - 1;
+                    if (!mbar_wait(&bar.p_full[gl & 1], (gl >> 1) & 1, abort, kWaitBudget)) ok = false;
+                    else {
+                        tc_fence_after();
+                        issue_pv(gl, n == 1);
+                    }
+                }
                 if (!ok) { fail(); break; }
                 mma_commit(&bar.o_final);
                 g += n;
@@ -430,9 +479,13 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                     }
                 }
                 // ---- online softmax (log2 domain) ------------------------------
-                float mx = -INFINITY;
+                float mx8[8];
 #pragma unroll
-                for (int c = 0; c < 64; ++c) mx = fmaxf(mx, s[c]);
+                for (int e = 0; e < 8; ++e) mx8[e] = s[e];
+#pragma unroll
+                for (int c = 8; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
                 const float ms = mx * a.scale_log2;
                 const bool need = ms > m + kRescaleThreshold;
                 const float m_new = need ? ms : m;
@@ -458,13 +511,14 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 }
                 const float base = (m == -INFINITY) ? 0.f : m;
                 unsigned char* ps = smem + C::kPOff + sb * C::kPBytes;
+                float lsum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8) {
                     float p[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         p[e] = fast_exp2(fmaf(s[c8 * 8 + e], a.scale_log2, -base));
-                        l += p[e];
+                        lsum[e] += p[e];
                     }
                     uint4 v;
                     v.x = pack_bf16(p[0], p[1]);
@@ -473,6 +527,8 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                     v.w = pack_bf16(p[6], p[7]);
                     *reinterpret_cast<uint4*>(ps + sw128(t, c8)) = v;
                 }
+                l += ((lsum[0] + lsum[1]) + (lsum[2] + lsum[3])) +
+                     ((lsum[4] + lsum[5]) + (lsum[6] + lsum[7]));
                 fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
@@ -671,9 +727,14 @@ cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, in
                                 const int64_t* ctx_offsets, int64_t total_kv, int max_kv,
                                 const int32_t* lens, const uint32_t* mask, int mask_words,
                                 void* o, void* workspace, int32_t* dev_status,
-                                cudaStream_t stream)
+                                cudaStream_t stream, const rd_paged_kv* paged)
 {
     TcArgs a;
+    a.block_table = paged ? paged->block_table : nullptr;
+    a.ctx_lens = paged ? paged->ctx_lens : nullptr;
+    a.max_pages = paged ? paged->max_pages : 0;
+    a.page_size = paged ? paged->page_size : 1;
+    a.num_pages = paged ? paged->num_pages : 0;
     a.causal = causal;
     a.B = B;
     a.P_max = P_max;
@@ -706,7 +767,7 @@ cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, in
     CUtensorMap mkc, mvc, mkd, mvd;
     const void* kc = causal ? k_new : k_cache;
     const void* vc = causal ? v_new : v_cache;
-    const int64_t kc_rows = total_kv;
+    const int64_t kc_rows = paged ? (int64_t)paged->num_pages * paged->page_size : total_kv;
     const int64_t kd_rows = causal ? total_kv : (int64_t)B * P_max;
     const void* kd = causal ? k_new : k_new;
     const void* vd = causal ? v_new : v_new;

@@ -81,6 +81,72 @@ rd_status rd_tree_attention(int B, int P_max, int Hq, int Hkv, int D, float scal
                                          dev_status, (cudaStream_t)stream));
 }
 
+rd_status rd_tree_attention_paged(int B, int P_max, int Hq, int Hkv, int D, float scale,
+                                  const void* q, const void* k_new, const void* v_new,
+                                  const void* k_pool, const void* v_pool, int num_pages,
+                                  int page_size, const int32_t* block_table, int max_pages,
+                                  const int32_t* ctx_lens, int max_ctx,
+                                  const int32_t* packed_len, const uint32_t* mask,
+                                  int mask_words, void* o, void* workspace, size_t ws_bytes,
+                                  int32_t* dev_status, rd_stream_t stream)
+{
+    if (B < 0 || P_max < 1 || !attn_shape_ok(Hq, Hkv, D) || num_pages < 0 || max_pages < 0 ||
+        max_ctx < 0 || page_size < 1)
+        return RD_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return RD_ERR_UNSUPPORTED;
+    if (page_size % 64 != 0) return RD_ERR_UNSUPPORTED;
+    if (P_max > RD_MAX_PACKED || B > 65535 || Hkv > 65535) return RD_ERR_UNSUPPORTED;
+    if ((long long)num_pages * page_size > 0x7fffffffLL) return RD_ERR_UNSUPPORTED;
+    if (mask_words != (P_max + 31) / 32) return RD_ERR_INVALID_ARG;
+    if (B == 0) return RD_OK;
+    if (!q || !k_new || !v_new || !block_table || !ctx_lens || !packed_len || !mask || !o)
+        return RD_ERR_INVALID_ARG;
+    if (num_pages > 0 && (!k_pool || !v_pool)) return RD_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) ||
+        !aligned16(v_pool) || !aligned16(o) || !aligned16(workspace))
+        return RD_ERR_INVALID_ARG;
+    const rd_attn_plan plan = rd_attn_make_plan(false, B, P_max, Hq, Hkv, D, max_ctx);
+    if (plan.ws_bytes > 0 && (!workspace || ws_bytes < plan.ws_bytes))
+        return RD_ERR_INVALID_ARG;
+    if (scale <= 0.f) scale = 1.0f / sqrtf((float)D);
+    rd_paged_kv pg;
+    pg.block_table = block_table;
+    pg.ctx_lens = ctx_lens;
+    pg.max_pages = max_pages;
+    pg.page_size = page_size;
+    pg.num_pages = num_pages;
+    return from_cuda(rd_launch_attention(false, plan, B, P_max, Hq, Hkv, D, scale, q, k_new,
+                                         v_new, num_pages > 0 ? k_pool : nullptr,
+                                         num_pages > 0 ? v_pool : nullptr, nullptr, 0, max_ctx,
+                                         packed_len, mask, mask_words, o, workspace,
+                                         dev_status, (cudaStream_t)stream, &pg));
+}
+
+rd_status rd_commit_accepted(int B, int W, int L, int P_max, int Hkv, int D,
+                             const void* k_new, const void* v_new, const int32_t* unpacker,
+                             const int32_t* best_beam, const int32_t* n_accepted,
+                             void* k_pool, void* v_pool, int num_pages, int page_size,
+                             const int32_t* block_table, int max_pages,
+                             const int32_t* ctx_lens, int32_t* new_ctx_lens,
+                             int32_t* dev_status, rd_stream_t stream)
+{
+    if (B < 0 || W < 1 || L < 1 || P_max < 1 || Hkv < 1 || num_pages < 0 || page_size < 1 ||
+        max_pages < 0)
+        return RD_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return RD_ERR_UNSUPPORTED;
+    if (B > 65535 || L > 65535) return RD_ERR_UNSUPPORTED;
+    if (B == 0) return RD_OK;
+    if (!k_new || !v_new || !unpacker || !best_beam || !n_accepted || !k_pool || !v_pool ||
+        !block_table || !ctx_lens || !new_ctx_lens || ctx_lens == new_ctx_lens)
+        return RD_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool))
+        return RD_ERR_INVALID_ARG;
+    return from_cuda(rd_launch_commit(B, W, L, P_max, Hkv, D, k_new, v_new, unpacker, best_beam,
+                                      n_accepted, k_pool, v_pool, num_pages, page_size,
+                                      block_table, max_pages, ctx_lens, new_ctx_lens, dev_status,
+                                      (cudaStream_t)stream));
+}
+
 rd_status rd_causal_attention(int B, int Hq, int Hkv, int D, float scale,
                               const void* q, const void* k, const void* v,
                               const int32_t* cu_seqlens, int64_t total_tokens,
@@ -146,6 +212,20 @@ rd_status rd_greedy_accept(const void* logits, int B, int P_max, int V,
                                              W, L, argmax, accept_len, best_beam, n_accepted,
                                              out_tokens, workspace, dev_status,
                                              (cudaStream_t)stream));
+}
+
+rd_status rd_beam_search_step(const void* logits, const float* scores_in,
+                              const int32_t* beams_in, int B, int W, int V, int t,
+                              int32_t* beams_out, float* scores_out, int32_t* parent,
+                              int32_t* dev_status, rd_stream_t stream)
+{
+    if (B < 0 || W < 1 || V < 1 || t < 0 || V < W) return RD_ERR_INVALID_ARG;
+    if (W > 16 || (long long)W * V > 0x7fffffffLL) return RD_ERR_UNSUPPORTED;
+    if (B == 0) return RD_OK;
+    if (!logits || !scores_in || (t > 0 && !beams_in) || !beams_out || !scores_out || !parent)
+        return RD_ERR_INVALID_ARG;
+    return from_cuda(rd_launch_beam_step(logits, scores_in, beams_in, B, W, V, t, beams_out,
+                                         scores_out, parent, dev_status, (cudaStream_t)stream));
 }
 
 }  // extern "C"

@@ -46,6 +46,11 @@ struct rd_attn_plan {
     int split_len;     // KV positions per split (multiple of the chunk size)
     size_t ws_bytes;   // workspace bytes needed
 };
+struct rd_paged_kv {
+    const int32_t* block_table;   // [B, max_pages]
+    const int32_t* ctx_lens;      // [B]
+    int max_pages, page_size, num_pages;
+};
 rd_attn_plan rd_attn_make_plan(bool causal, int B, int P_max, int Hq, int Hkv, int D,
                                int max_kv);
 cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, int P_max,
@@ -55,4 +60,16 @@ cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, in
                                 const int64_t* ctx_offsets, int64_t total_kv, int max_kv,
                                 const int32_t* lens, const uint32_t* mask, int mask_words,
                                 void* o, void* workspace, int32_t* dev_status,
-                                cudaStream_t stream);
+                                cudaStream_t stream, const rd_paged_kv* paged = nullptr);
+
+cudaError_t rd_launch_commit(int B, int W, int L, int P_max, int Hkv, int D, const void* k_new,
+                             const void* v_new, const int32_t* unpacker,
+                             const int32_t* best_beam, const int32_t* n_accepted, void* k_pool,
+                             void* v_pool, int num_pages, int page_size,
+                             const int32_t* block_table, int max_pages, const int32_t* ctx_lens,
+                             int32_t* new_ctx_lens, int32_t* dev_status, cudaStream_t stream);
+
+cudaError_t rd_launch_beam_step(const void* logits, const float* scores_in,
+                                const int32_t* beams_in, int B, int W, int V, int t,
+                                int32_t* beams_out, float* scores_out, int32_t* parent,
+                                int32_t* dev_status, cudaStream_t stream);

@@ -283,3 +283,38 @@ def make_mixed_inputs(split: str = "mixed", device="cpu", scale: float = 1.0,
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """Raw bf16 bit patterns of a tensor as a host uint16 array (no rounding)."""
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def make_paged(k_cache: torch.Tensor, v_cache: torch.Tensor, ctx_lens, page_size: int,
+               rng: np.random.Generator, spare_pages: int = 2, spare_slots: int = 1) -> dict:
+    """Scatter a contiguous ragged cache [sum C, Hkv, D] into a paged pool
+    [num_pages, page_size, Hkv, D] whose pages are assigned in a random order.
+    Each request gets `spare_slots` extra pages in its block table (room to append)
+    and the pool holds `spare_pages` pages nobody uses; unused pool rows and
+    table slots hold random junk."""
+    lens = np.asarray(ctx_lens, np.int64)
+    B = len(lens)
+    need = [int(-(-int(c) // page_size)) + spare_slots for c in lens]
+    max_pages = max(need) if B else 1
+    n_pages = int(sum(need)) + spare_pages
+    perm = rng.permutation(n_pages).astype(np.int32)
+    table = rng.integers(-5, n_pages + 5, size=(B, max_pages)).astype(np.int32)
+    Hkv, D = k_cache.shape[1], k_cache.shape[2]
+    dev = k_cache.device
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(int(rng.integers(1 << 31)))
+    k_pool = _randn_bf16((n_pages, page_size, Hkv, D), gen, dev)
+    v_pool = _randn_bf16((n_pages, page_size, Hkv, D), gen, dev)
+    off, k = 0, 0
+    for b in range(B):
+        table[b, :need[b]] = perm[k:k + need[b]]
+        k += need[b]
+        C = int(lens[b])
+        for slot in range(-(-C // page_size)):
+            n = min(page_size, C - slot * page_size)
+            pg = int(table[b, slot])
+            k_pool[pg, :n] = k_cache[off + slot * page_size: off + slot * page_size + n]
+            v_pool[pg, :n] = v_cache[off + slot * page_size: off + slot * page_size + n]
+        off += C
+    return dict(k_pool=k_pool, v_pool=v_pool, block_table=torch.from_numpy(table).to(dev),
+                ctx_lens=torch.from_numpy(lens.astype(np.int32)).to(dev), page_size=page_size)
