@@ -147,6 +147,28 @@ rd_status rd_tree_attention(int B, int P_max, int Hq, int Hkv, int D, float scal
                             int32_t* dev_status, rd_stream_t stream);
 
 /*
+ * rd_tree_attention_fp8 -- rd_tree_attention with the context K/V cache stored
+ * in FP8 (e4m3) with one scale per tensor (TensorRT-LLM's FP8 quantisation:
+ * NVIDIA blog "ReDrafter in TensorRT-LLM", introduction).  Context key j is
+ * k_scale * e4m3(k_cache[j]) and likewise for values; the packed drafts stay
+ * bf16.  Same computation, outputs and workspace as rd_tree_attention.
+ *
+ * k_cache,v_cache uint8 e4m3 bit patterns [total_ctx, Hkv, D]
+ * k_scale,v_scale finite, > 0
+ * Supported: D = 128, total_ctx >= 1 (RD_ERR_UNSUPPORTED otherwise).
+ * The contraction runs in f16 (every e4m3 value and every bf16 query is
+ * exact in f16 within f16's range; draft K/V are divided by the scales and
+ * rounded to f16).
+ */
+rd_status rd_tree_attention_fp8(int B, int P_max, int Hq, int Hkv, int D, float scale,
+                                const void* q, const void* k_new, const void* v_new,
+                                const void* k_cache, const void* v_cache, float k_scale,
+                                float v_scale, const int64_t* ctx_offsets, int64_t total_ctx,
+                                int max_ctx, const int32_t* packed_len, const uint32_t* mask,
+                                int mask_words, void* o, void* workspace, size_t ws_bytes,
+                                int32_t* dev_status, rd_stream_t stream);
+
+/*
  * rd_tree_attention_paged -- rd_tree_attention with the context in a paged KV
  * cache (TensorRT-LLM's paged KV caching: NVIDIA blog "ReDrafter in
  * TensorRT-LLM", introduction).  Same computation, outputs and workspace as

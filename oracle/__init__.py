@@ -56,9 +56,15 @@ def _load():
                                                         P, P, I, I, P, I, P, P, P, I, P, I]
             lib.oracle_greedy_accept.argtypes = [P, I, I, I, P, P, P, I, I, P, P, P, P, P]
             lib.oracle_beam_search_step.argtypes = [P, P, P, I, I, I, I, P, P, P]
+            lib.oracle_tree_attention_fp8.argtypes = [I, I, I, I, I, ctypes.c_double, P, P, P, P,
+                                                      P, ctypes.c_double, ctypes.c_double, P, P,
+                                                      P, I, P]
+            lib.oracle_e4m3_value.argtypes = [I]
+            lib.oracle_e4m3_value.restype = ctypes.c_double
             for f in (lib.oracle_pack, lib.oracle_tree_attention,
                       lib.oracle_tree_attention_paged, lib.oracle_causal_attention,
-                      lib.oracle_greedy_accept, lib.oracle_beam_search_step):
+                      lib.oracle_greedy_accept, lib.oracle_beam_search_step,
+                      lib.oracle_tree_attention_fp8):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -140,6 +146,32 @@ def oracle_tree_attention_paged(q, k_new, v_new, k_pool, v_pool, block_table, ct
         n_threads or n_threads_default())
     if rc != 0:
         raise ValueError(f"oracle_tree_attention_paged rejected the input (rc={rc})")
+    return o
+
+
+def oracle_e4m3_value(code: int) -> float:
+    """The value of an e4m3 bit pattern (see e4m3_to_f64 in rd_oracle.c)."""
+    return float(_load().oracle_e4m3_value(int(code)))
+
+
+def oracle_tree_attention_fp8(q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, ctx_offsets,
+                              packed_len, mask, scale: float = 0.0) -> np.ndarray:
+    """Tree-masked attention with e4m3 context K/V (uint8 bit patterns
+    [sum C, Hkv, D]) and per-tensor scales; q/k_new/v_new bf16 bits as in
+    oracle_tree_attention.  Returns float64 [B, P, Hq, D]."""
+    q = _c(q, np.uint16); k_new = _c(k_new, np.uint16); v_new = _c(v_new, np.uint16)
+    k_cache = _c(k_cache, np.uint8); v_cache = _c(v_cache, np.uint8)
+    ctx_offsets = _c(ctx_offsets, np.int64); packed_len = _c(packed_len, np.int32)
+    mask = _c(mask, np.uint32)
+    B, P, Hq, D = q.shape
+    Hkv = k_new.shape[2]
+    o = np.zeros((B, P, Hq, D), np.float64)
+    rc = _load().oracle_tree_attention_fp8(B, P, Hq, Hkv, D, float(scale), _ptr(q), _ptr(k_new),
+                                           _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                           float(k_scale), float(v_scale), _ptr(ctx_offsets),
+                                           _ptr(packed_len), _ptr(mask), mask.shape[2], _ptr(o))
+    if rc != 0:
+        raise ValueError(f"oracle_tree_attention_fp8 rejected the input (rc={rc})")
     return o
 
 

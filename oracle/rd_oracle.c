@@ -25,6 +25,9 @@
  *                          TensorRT-LLM's paged KV caching): position j of
  *                          request b lives in page block_table[b][j / page_size],
  *                          row j % page_size.
+ *   oracle_tree_attention_fp8  the same attention with the context K/V stored
+ *                          as e4m3 with one scale per tensor (NVIDIA blog,
+ *                          introduction: TensorRT-LLM's FP8 quantisation).
  *   oracle_causal_attention  causal prefill of context-phase requests (NVIDIA
  *                          blog, "Inflight-batching Compatible Engine").
  *   oracle_beam_search_step  one step of the drafter's beam search (news page,
@@ -473,5 +476,95 @@ int oracle_beam_search_step(const uint16_t* logits, const double* scores_in,
     }
     free(cand);
     free(taken);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* FP8 (e4m3) context                                                        */
+/* ------------------------------------------------------------------------ */
+/* e4m3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; exponent 0 is
+ * subnormal (m/8 * 2^-6); S.1111.111 is NaN; there are no infinities. */
+static double e4m3_to_f64(uint8_t x)
+{
+    int sgn = x >> 7, e = (x >> 3) & 15, m = x & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m / 8.0, -6);
+    else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sgn ? -v : v;
+}
+
+double oracle_e4m3_value(int code) { return e4m3_to_f64((uint8_t)code); }
+
+int oracle_tree_attention_fp8(int B, int P_max, int Hq, int Hkv, int D, double scale,
+                              const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                              const uint8_t* k_cache, const uint8_t* v_cache, double k_scale,
+                              double v_scale, const int64_t* ctx_offsets,
+                              const int32_t* packed_len, const uint32_t* mask, int mask_words,
+                              double* o)
+{
+    if (B < 0 || P_max <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0) return -1;
+    if (scale <= 0) scale = 1.0 / sqrt((double)D);
+    int G = Hq / Hkv;
+    int64_t max_n = 0;
+    for (int b = 0; b < B; ++b) {
+        if (packed_len[b] < 0 || packed_len[b] > P_max) return -1;
+        int64_t c = ctx_offsets[b + 1] - ctx_offsets[b] + P_max;
+        if (c > max_n) max_n = c;
+    }
+    double* s_buf = malloc(sizeof(double) * (size_t)(max_n + 1));
+    if (!s_buf) return -3;
+    for (int b = 0; b < B; ++b) {
+        int64_t c0 = ctx_offsets[b], C = ctx_offsets[b + 1] - c0;
+        int Pb = packed_len[b];
+        for (int hq = 0; hq < Hq; ++hq) {
+            int h = hq / G;
+            for (int p = 0; p < P_max; ++p) {
+                double* out = o + (((size_t)b * P_max + p) * Hq + hq) * D;
+                for (int d = 0; d < D; ++d) out[d] = 0.0;
+                if (p >= Pb) continue;
+                const uint16_t* qv = q + (((size_t)b * P_max + p) * Hq + hq) * D;
+                const uint32_t* row = mask + ((size_t)b * P_max + p) * mask_words;
+                /* scores: context keys are k_scale * e4m3, drafts are bf16 */
+                double m = -INFINITY;
+                int64_t n = 0;
+                for (int64_t j = 0; j < C; ++j, ++n) {
+                    const uint8_t* kr = k_cache + ((size_t)(c0 + j) * Hkv + h) * D;
+                    double sc = 0.0;
+                    for (int d = 0; d < D; ++d) sc += bf16_to_f64(qv[d]) * (k_scale * e4m3_to_f64(kr[d]));
+                    s_buf[n] = sc * scale;
+                    if (s_buf[n] > m) m = s_buf[n];
+                }
+                for (int k = 0; k < Pb; ++k) {
+                    if (!(row[k / 32] & (1u << (k % 32)))) continue;
+                    const uint16_t* kr = k_new + (((size_t)b * P_max + k) * Hkv + h) * D;
+                    double sc = 0.0;
+                    for (int d = 0; d < D; ++d) sc += bf16_to_f64(qv[d]) * bf16_to_f64(kr[d]);
+                    s_buf[n] = sc * scale;
+                    if (s_buf[n] > m) m = s_buf[n];
+                    ++n;
+                }
+                /* softmax-weighted values, in the same order */
+                double l = 0.0;
+                n = 0;
+                for (int64_t j = 0; j < C; ++j, ++n) {
+                    double e = exp(s_buf[n] - m);
+                    const uint8_t* vr = v_cache + ((size_t)(c0 + j) * Hkv + h) * D;
+                    l += e;
+                    for (int d = 0; d < D; ++d) out[d] += e * (v_scale * e4m3_to_f64(vr[d]));
+                }
+                for (int k = 0; k < Pb; ++k) {
+                    if (!(row[k / 32] & (1u << (k % 32)))) continue;
+                    double e = exp(s_buf[n] - m);
+                    const uint16_t* vr = v_new + (((size_t)b * P_max + k) * Hkv + h) * D;
+                    l += e;
+                    for (int d = 0; d < D; ++d) out[d] += e * bf16_to_f64(vr[d]);
+                    ++n;
+                }
+                for (int d = 0; d < D; ++d) out[d] /= l;
+            }
+        }
+    }
+    free(s_buf);
     return 0;
 }

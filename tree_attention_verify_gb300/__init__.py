@@ -22,7 +22,8 @@ __all__ = [
     "rd_pack_beams", "rd_tree_attention", "rd_tree_attention_workspace_size",
     "rd_causal_attention", "rd_unpack", "rd_greedy_accept",
     "rd_greedy_accept_workspace_size", "rd_greedy_accept_noalloc",
-    "rd_tree_attention_paged", "rd_commit_accepted", "rd_beam_search_step", "RdError", "DEV_BAD_INDEX", "DEV_BAD_TOKEN",
+    "rd_tree_attention_paged", "rd_commit_accepted", "rd_beam_search_step",
+    "rd_tree_attention_fp8", "RdError", "DEV_BAD_INDEX", "DEV_BAD_TOKEN",
     "DEV_OVERFLOW", "DEV_BAD_LENGTH", "DEV_TIMEOUT", "lib_path",
 ]
 
@@ -60,6 +61,8 @@ def _load() -> ctypes.CDLL:
                                     P, P, S, P, P],
         "rd_commit_accepted": [I, I, I, I, I, I, P, P, P, P, P, P, P, I, I, P, I, P, P, P, P],
         "rd_beam_search_step": [P, P, P, I, I, I, I, P, P, P, P, P],
+        "rd_tree_attention_fp8": [I, I, I, I, I, F, P, P, P, P, P, F, F, P, I64, I, P, P, I, P, P,
+                                  S, P, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -176,6 +179,41 @@ def rd_tree_attention(q, k_new, v_new, k_cache, v_cache, ctx_offsets, packed_len
         B, P, Hq, Hkv, D, float(scale), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
         _ptr(v_cache), _ptr(ctx_offsets), int(k_cache.shape[0]), int(max_ctx), _ptr(packed_len),
         _ptr(mask), int(mask.shape[2]), _ptr(out), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(),
+        _ptr(dev_status), _stream(stream)))
+    return out
+
+
+def rd_tree_attention_fp8(q, k_new, v_new, k_cache, v_cache, k_scale: float, v_scale: float,
+                          ctx_offsets, packed_len, mask, *, max_ctx: int, scale: float = 0.0,
+                          out=None, workspace=None, dev_status=None, stream=None) -> torch.Tensor:
+    """rd_tree_attention with an e4m3 context cache: k_cache/v_cache uint8 (or
+    float8_e4m3fn) [total_ctx, Hkv, D] holding e4m3 bit patterns, per-tensor
+    scales k_scale/v_scale (see rd_tree_attention_fp8 in rd.h)."""
+    for n, t in (("q", q), ("k_new", k_new), ("v_new", v_new)):
+        _need(t, n, torch.bfloat16, ndim=4)
+    if k_cache.dtype != torch.uint8:
+        k_cache = k_cache.view(torch.uint8)
+    if v_cache.dtype != torch.uint8:
+        v_cache = v_cache.view(torch.uint8)
+    _need(k_cache, "k_cache", torch.uint8, ndim=3)
+    _need(v_cache, "v_cache", torch.uint8, ndim=3)
+    _need(ctx_offsets, "ctx_offsets", torch.int64, ndim=1)
+    _need(packed_len, "packed_len", torch.int32, ndim=1)
+    B, P, Hq, D = q.shape
+    Hkv = k_new.shape[2]
+    if k_cache.shape[1:] != (Hkv, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache/v_cache must be [total_ctx, Hkv, D]")
+    if out is None:
+        out = torch.empty_like(q)
+    ws_need = rd_tree_attention_workspace_size(B, P, Hq, Hkv, D, max_ctx)
+    if ws_need and workspace is None:
+        workspace = torch.zeros(ws_need, dtype=torch.uint8, device=q.device)
+    _check("rd_tree_attention_fp8", _lib.rd_tree_attention_fp8(
+        B, P, Hq, Hkv, D, float(scale), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+        _ptr(v_cache), float(k_scale), float(v_scale), _ptr(ctx_offsets),
+        int(k_cache.shape[0]), int(max_ctx), _ptr(packed_len), _ptr(mask), int(mask.shape[2]),
+        _ptr(out), _ptr(workspace),
         0 if workspace is None else workspace.numel() * workspace.element_size(),
         _ptr(dev_status), _stream(stream)))
     return out

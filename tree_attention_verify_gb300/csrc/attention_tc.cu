@@ -24,10 +24,18 @@
 //              ring of stages.
 //   warp 5     MMA issuer: S = Q K^T (M=128, N=64, K=D) into a double-buffered
 //              TMEM tile, then O += P V (M=128, N=D, K=64) into TMEM.
+// FP8 variant (template flag F8; context K/V stored as e4m3 with per-tensor
+// scales): the producer TMA-loads e4m3 context chunks into an 8-bit ring; four
+// more warps (6-9) widen them (exactly) into the 16-bit ring the MMA reads, and
+// convert the bf16 draft chunks, divided by the scales, the same way.  The MMA
+// then runs kind::f16 with f16 operands (e4m3 widens to f16 exactly and both
+// operands of one MMA share a type); the K scale is folded into the softmax
+// scale and the V scale into the output normalisation.
 // Every wait is bounded by a clock budget; on expiry the CTA records
 // RD_DEV_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -42,23 +50,28 @@ constexpr int kM = 128;                    // query rows per tile = TMEM lanes
 constexpr int kN = 64;                     // KV positions per chunk
 constexpr int kSoftmaxThreads = 128;
 constexpr int kThreads = kSoftmaxThreads + 64;
+constexpr int kThreadsF8 = kThreads + 128;   // + four converter warps
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
+constexpr int kConvWarp0 = 6;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when a max grows by > 2^8
 constexpr long long kWaitBudget = 4000000000LL;   // ~2 s of SM clock per wait
 
-template <int D> struct Cfg {
+template <int D, bool F8 = false> struct Cfg {
     static constexpr int kDB = D / 64;                  // 64-element (128-byte) column blocks
-    static constexpr int kStages = D == 128 ? 5 : 8;
+    static constexpr int kStages = F8 ? 3 : (D == 128 ? 5 : 8);   // 16-bit ring
+    static constexpr int kF8Stages = F8 ? 4 : 0;        // 8-bit ring (context chunks)
     static constexpr int kQBytes = kM * D * 2;
     static constexpr int kPBytes = kM * kN * 2;         // one probability buffer
     static constexpr int kKBytes = kN * D * 2;          // one K (or V) chunk
     static constexpr int kStageBytes = 2 * kKBytes;
+    static constexpr int kF8Bytes = 2 * kN * D;         // one 8-bit K + V chunk
     static constexpr int kQOff = 0;
     static constexpr int kPOff = kQOff + kQBytes;
     static constexpr int kStageOff = kPOff + 2 * kPBytes;
-    static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
+    static constexpr int kF8Off = kStageOff + kStages * kStageBytes;
+    static constexpr int kBarOff = kF8Off + kF8Stages * kF8Bytes;
     static constexpr int kSmemBytes = kBarOff + 512 + 1024;   // + barriers + alignment slack
     static constexpr uint32_t kTmemCols = 256;          // S: 2 x 64, O: D (<= 128)
     static constexpr uint32_t kSCol = 0;
@@ -85,6 +98,11 @@ struct TcArgs {
     const int32_t* block_table;
     const int32_t* ctx_lens;
     int max_pages, page_size, num_pages;
+    // FP8 variant: draft K/V (bf16, converted by the converter warps), the
+    // reciprocal scales applied to them, and the V scale of the output
+    const uint16_t* k_new;
+    const uint16_t* v_new;
+    float k_inv, v_inv, out_scale;
 };
 
 struct Barriers {
@@ -97,6 +115,8 @@ struct Barriers {
     uint64_t o_final;
     uint64_t q_full;
     uint64_t drain;
+    uint64_t f8_full[4];
+    uint64_t f8_empty[4];
     uint32_t tmem_base;
     int abort;
 };
@@ -188,6 +208,32 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+template <bool F8>
+__device__ __forceinline__ uint32_t pack16(float lo, float hi)
+{
+    if constexpr (F8) {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    } else {
+        return pack_bf16(lo, hi);
+    }
+}
+
+// two bf16 (one 32-bit word) times a scale, as two f16
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, float scale)
+{
+    return pack16<true>(__uint_as_float(w << 16) * scale, __uint_as_float(w & 0xffff0000u) * scale);
+}
+
+// two e4m3 values (one 16-bit word) to two f16, exactly
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w16)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b16 t;\n\tmov.b16 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+        : "=r"(r) : "h"((unsigned short)w16));
+    return r;
+}
+
 // 2^x with the hardware approximation (ex2.approx; 2^-inf = 0)
 __device__ __forceinline__ float fast_exp2(float x)
 {
@@ -205,14 +251,14 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, ok);
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, bool F8>
+__global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
 tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map_kc,
                          const __grid_constant__ CUtensorMap map_vc,
                          const __grid_constant__ CUtensorMap map_kd,
                          const __grid_constant__ CUtensorMap map_vd)
 {
-    using C = Cfg<D>;
+    using C = Cfg<D, F8>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -226,8 +272,12 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
 
     if (tid == 0) {
         for (int i = 0; i < C::kStages; ++i) {
-            mbar_init(&bar.kv_full[i], 1);
+            mbar_init(&bar.kv_full[i], F8 ? 4 : 1);        // F8: the four converter warps
             mbar_init(&bar.kv_empty[i], 1);
+        }
+        for (int i = 0; i < C::kF8Stages; ++i) {
+            mbar_init(&bar.f8_full[i], 1);
+            mbar_init(&bar.f8_empty[i], 4);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bar.s_full[i], 1);
@@ -261,7 +311,99 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
         rd_flag(a.status, RD_DEV_TIMEOUT);
     };
 
-    if (warp == kProducerWarp) {
+    if (F8 && warp == kProducerWarp) {
+        // ------------------------------------------------- producer (8-bit context)
+        if (lane == 0) {
+            uint32_t g8 = 0;                              // context chunks only
+            for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
+                const UnitGeo geo = unit_geo(a, u);
+                if (!geo.live) continue;
+                bool ok = true;
+                for (int j = 0; j < geo.n_ctx; ++j, ++g8) {
+                    const int st = g8 % C::kF8Stages;
+                    if (g8 >= (uint32_t)C::kF8Stages &&
+                        !mbar_wait(&bar.f8_empty[st], ((g8 / C::kF8Stages) - 1) & 1, abort, kWaitBudget)) {
+                        ok = false;
+                        break;
+                    }
+                    unsigned char* dst = smem + C::kF8Off + st * C::kF8Bytes;
+                    mbar_arrive_expect_tx(&bar.f8_full[st], C::kF8Bytes);
+                    const int z = (int)(geo.kv_base + (int64_t)(geo.c_first + j) * kN);
+                    tma_load_3d(dst, &map_kc, &bar.f8_full[st], 0, geo.h, z);
+                    tma_load_3d(dst + kN * D, &map_vc, &bar.f8_full[st], 0, geo.h, z);
+                }
+                if (!ok) { fail(); break; }
+            }
+            const uint32_t first = g8 > (uint32_t)C::kF8Stages ? g8 - C::kF8Stages : 0u;
+            for (uint32_t k = first; k < g8; ++k)
+                mbar_wait(&bar.f8_full[k % C::kF8Stages], (k / C::kF8Stages) & 1, &no_abort, kWaitBudget);
+        }
+    } else if (F8 && warp >= kConvWarp0) {
+        // ------------------------------------------------------------ converters
+        // thread ct: row ct % 64 of K (ct < 64) or V of every chunk
+        const int ct = tid - kConvWarp0 * 32;
+        const int is_v = ct >> 6, row = ct & 63;
+        uint32_t g = 0, g8 = 0;
+        for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
+            const UnitGeo geo = unit_geo(a, u);
+            if (!geo.live) continue;
+            const int n = geo.n_ctx + geo.n_draft;
+            bool ok = true;
+            for (int j = 0; j < n; ++j, ++g) {
+                const int st = g % C::kStages;
+                if (g >= (uint32_t)C::kStages &&
+                    !warp_wait(&bar.kv_empty[st], ((g / C::kStages) - 1) & 1, abort, kWaitBudget)) {
+                    ok = false;
+                    break;
+                }
+                unsigned char* dst = smem + C::kStageOff + st * C::kStageBytes + is_v * C::kKBytes;
+                if (j < geo.n_ctx) {
+                    const int s8 = g8 % C::kF8Stages;
+                    if (!warp_wait(&bar.f8_full[s8], (g8 / C::kF8Stages) & 1, abort, kWaitBudget)) {
+                        ok = false;
+                        break;
+                    }
+                    const unsigned char* src = smem + C::kF8Off + s8 * C::kF8Bytes + is_v * (kN * D);
+#pragma unroll
+                    for (int c = 0; c < D / 16; ++c) {      // 16 e4m3 values = 16 B (swizzled row)
+                        const uint4 x = *reinterpret_cast<const uint4*>(src + sw128(row, c));
+                        uint4 lo, hi;
+                        lo.x = e4m3x2_to_f16x2(x.x & 0xffffu); lo.y = e4m3x2_to_f16x2(x.x >> 16);
+                        lo.z = e4m3x2_to_f16x2(x.y & 0xffffu); lo.w = e4m3x2_to_f16x2(x.y >> 16);
+                        hi.x = e4m3x2_to_f16x2(x.z & 0xffffu); hi.y = e4m3x2_to_f16x2(x.z >> 16);
+                        hi.z = e4m3x2_to_f16x2(x.w & 0xffffu); hi.w = e4m3x2_to_f16x2(x.w >> 16);
+                        const int c16 = 2 * c;              // two 16-bit chunks of 8 values
+                        *reinterpret_cast<uint4*>(dst + (c16 >> 3) * (kN * 128) + sw128(row, c16 & 7)) = lo;
+                        *reinterpret_cast<uint4*>(dst + ((c16 + 1) >> 3) * (kN * 128) + sw128(row, (c16 + 1) & 7)) = hi;
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar.f8_empty[s8]);
+                    ++g8;
+                } else {
+                    const int d = (j - geo.n_ctx) * kN + row;   // draft row
+                    const float sc = is_v ? a.v_inv : a.k_inv;
+                    const uint4* src = d < geo.Pb
+                        ? reinterpret_cast<const uint4*>((is_v ? a.v_new : a.k_new) +
+                                                         (((size_t)geo.b * a.P_max + d) * a.Hkv + geo.h) * D)
+                        : nullptr;
+#pragma unroll
+                    for (int c = 0; c < D / 8; ++c) {
+                        uint4 y = make_uint4(0, 0, 0, 0);
+                        if (src) {
+                            const uint4 x = __ldg(src + c);
+                            y.x = bf16x2_to_f16x2(x.x, sc); y.y = bf16x2_to_f16x2(x.y, sc);
+                            y.z = bf16x2_to_f16x2(x.z, sc); y.w = bf16x2_to_f16x2(x.w, sc);
+                        }
+                        *reinterpret_cast<uint4*>(dst + (c >> 3) * (kN * 128) + sw128(row, c & 7)) = y;
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar.kv_full[st]);
+            }
+            if (!ok) { fail(); break; }
+        }
+    } else if (!F8 && warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             uint32_t g = 0;                               // global chunk counter
@@ -317,8 +459,8 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idS = idesc_bf16(kM, kN, false, false);
-            constexpr uint32_t idPV = idesc_bf16(kM, D, false, true);
+            constexpr uint32_t idS = F8 ? idesc_f16(kM, kN, false, false) : idesc_bf16(kM, kN, false, false);
+            constexpr uint32_t idPV = F8 ? idesc_f16(kM, D, false, true) : idesc_bf16(kM, D, false, true);
             uint32_t g = 0, unit_iter = 0;
             // Shared-memory descriptors differ only in their start-address field
             // (bits 0-13, address >> 4): build each base once and add offsets,
@@ -429,7 +571,11 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 unsigned char* qs = smem + C::kQOff;
 #pragma unroll
                 for (int c = 0; c < D / 8; ++c) {
-                    const uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+                    uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+                    if constexpr (F8) {
+                        v.x = bf16x2_to_f16x2(v.x, 1.f); v.y = bf16x2_to_f16x2(v.y, 1.f);
+                        v.z = bf16x2_to_f16x2(v.z, 1.f); v.w = bf16x2_to_f16x2(v.w, 1.f);
+                    }
                     *reinterpret_cast<uint4*>(qs + (c >> 3) * (kM * 128) + sw128(t, c & 7)) = v;
                 }
                 fence_proxy_async_smem();
@@ -521,10 +667,10 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                         lsum[e] += p[e];
                     }
                     uint4 v;
-                    v.x = pack_bf16(p[0], p[1]);
-                    v.y = pack_bf16(p[2], p[3]);
-                    v.z = pack_bf16(p[4], p[5]);
-                    v.w = pack_bf16(p[6], p[7]);
+                    v.x = pack16<F8>(p[0], p[1]);
+                    v.y = pack16<F8>(p[2], p[3]);
+                    v.z = pack16<F8>(p[4], p[5]);
+                    v.w = pack16<F8>(p[6], p[7]);
                     *reinterpret_cast<uint4*>(ps + sw128(t, c8)) = v;
                 }
                 l += ((lsum[0] + lsum[1]) + (lsum[2] + lsum[3])) +
@@ -539,7 +685,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             // ---- epilogue ----------------------------------------------------------
             const bool split_mode = !a.causal && geo.n_splits > 1;
             if (!split_mode) {
-                const float inv = (valid && l > 0.f) ? 1.f / l : 0.f;
+                const float inv = (valid && l > 0.f) ? a.out_scale / l : 0.f;
                 const bool write = valid || (!a.causal && qpos < a.P_max);
                 uint16_t* dst = nullptr;
                 if (write) {
@@ -616,7 +762,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                                     acc[4] += x1.x * w; acc[5] += x1.y * w; acc[6] += x1.z * w; acc[7] += x1.w * w;
                                 }
                             }
-                            const float inv = (valid && Ls > 0.f) ? 1.f / Ls : 0.f;
+                            const float inv = (valid && Ls > 0.f) ? a.out_scale / Ls : 0.f;
                             uint4 v;
                             v.x = pack_bf16(acc[0] * inv, acc[1] * inv);
                             v.y = pack_bf16(acc[2] * inv, acc[3] * inv);
@@ -668,6 +814,22 @@ bool make_kv_map(CUtensorMap* map, const void* base, int64_t rows, int heads, in
     cuuint32_t box[3] = {64, 1, (cuuint32_t)kN};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// [rows, heads, D] e4m3 -> boxes of 64 positions x 1 head x D bytes, 128-byte swizzle
+bool make_fp8_map(CUtensorMap* map, const void* base, int64_t rows, int heads, int D)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)D, (cuuint64_t)heads * D};
+    cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)kN};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -727,7 +889,8 @@ cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, in
                                 const int64_t* ctx_offsets, int64_t total_kv, int max_kv,
                                 const int32_t* lens, const uint32_t* mask, int mask_words,
                                 void* o, void* workspace, int32_t* dev_status,
-                                cudaStream_t stream, const rd_paged_kv* paged)
+                                cudaStream_t stream, const rd_paged_kv* paged,
+                                const rd_fp8_kv* fp8)
 {
     TcArgs a;
     a.block_table = paged ? paged->block_table : nullptr;
@@ -758,6 +921,15 @@ cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, in
     a.o_part = nullptr;
     a.ml_part = nullptr;
     a.tickets = nullptr;
+    a.k_new = static_cast<const uint16_t*>(k_new);
+    a.v_new = static_cast<const uint16_t*>(v_new);
+    a.k_inv = a.v_inv = a.out_scale = 1.f;
+    if (fp8 != nullptr) {
+        a.k_inv = 1.f / fp8->k_scale;
+        a.v_inv = 1.f / fp8->v_scale;
+        a.out_scale = fp8->v_scale;
+        a.scale_log2 *= fp8->k_scale;
+    }
     if (plan.splits > 1) {
         const size_t unit_rows = (size_t)B * Hkv * plan.tiles * kM;
         a.o_part = static_cast<float*>(workspace);
@@ -772,25 +944,40 @@ cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, in
     const void* kd = causal ? k_new : k_new;
     const void* vd = causal ? v_new : v_new;
     if (kc == nullptr || kc_rows == 0) { kc = kd; vc = vd; }
+    const int grid = (int)std::min<long>((long)a.n_units, (long)num_sms());
+    if (fp8 != nullptr) {
+        // 8-bit context maps (the drafts are read by the converter warps)
+        if (D != 128 || causal || paged || total_kv < 1 ||
+            !make_fp8_map(&mkc, fp8->k_cache, total_kv, Hkv, D) ||
+            !make_fp8_map(&mvc, fp8->v_cache, total_kv, Hkv, D))
+            return cudaErrorInvalidValue;
+        using Cf = Cfg<128, true>;
+        cudaError_t e = cudaFuncSetAttribute(tree_attention_tc_kernel<128, true>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Cf::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        tree_attention_tc_kernel<128, true><<<grid, kThreadsF8, Cf::kSmemBytes, stream>>>(
+            a, mkc, mvc, mkc, mvc);
+        return cudaGetLastError();
+    }
     if (!make_kv_map(&mkc, kc, kc_rows > 0 ? kc_rows : kd_rows, Hkv, D) ||
         !make_kv_map(&mvc, vc, kc_rows > 0 ? kc_rows : kd_rows, Hkv, D) ||
         !make_kv_map(&mkd, kd, kd_rows, Hkv, D) || !make_kv_map(&mvd, vd, kd_rows, Hkv, D))
         return cudaErrorInvalidValue;
-    const int grid = (int)std::min<long>((long)a.n_units, (long)num_sms());
     if (D == 128) {
         using Cf = Cfg<128>;
-        cudaError_t e = cudaFuncSetAttribute(tree_attention_tc_kernel<128>,
+        cudaError_t e = cudaFuncSetAttribute(tree_attention_tc_kernel<128, false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Cf::kSmemBytes);
         if (e != cudaSuccess) return e;
-        tree_attention_tc_kernel<128><<<grid, kThreads, Cf::kSmemBytes, stream>>>(a, mkc, mvc, mkd, mvd);
+        tree_attention_tc_kernel<128, false><<<grid, kThreads, Cf::kSmemBytes, stream>>>(a, mkc, mvc, mkd, mvd);
     } else {
         using Cf = Cfg<64>;
-        cudaError_t e = cudaFuncSetAttribute(tree_attention_tc_kernel<64>,
+        cudaError_t e = cudaFuncSetAttribute(tree_attention_tc_kernel<64, false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Cf::kSmemBytes);
         if (e != cudaSuccess) return e;
-        tree_attention_tc_kernel<64><<<grid, kThreads, Cf::kSmemBytes, stream>>>(a, mkc, mvc, mkd, mvd);
+        tree_attention_tc_kernel<64, false><<<grid, kThreads, Cf::kSmemBytes, stream>>>(a, mkc, mvc, mkd, mvd);
     }
     return cudaGetLastError();
 }

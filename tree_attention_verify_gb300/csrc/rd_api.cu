@@ -81,6 +81,44 @@ rd_status rd_tree_attention(int B, int P_max, int Hq, int Hkv, int D, float scal
                                          dev_status, (cudaStream_t)stream));
 }
 
+rd_status rd_tree_attention_fp8(int B, int P_max, int Hq, int Hkv, int D, float scale,
+                                const void* q, const void* k_new, const void* v_new,
+                                const void* k_cache, const void* v_cache, float k_scale,
+                                float v_scale, const int64_t* ctx_offsets, int64_t total_ctx,
+                                int max_ctx, const int32_t* packed_len, const uint32_t* mask,
+                                int mask_words, void* o, void* workspace, size_t ws_bytes,
+                                int32_t* dev_status, rd_stream_t stream)
+{
+    if (B < 0 || P_max < 1 || !attn_shape_ok(Hq, Hkv, D) || total_ctx < 0 || max_ctx < 0)
+        return RD_ERR_INVALID_ARG;
+    if (!(k_scale > 0.f) || !(v_scale > 0.f) || !isfinite(k_scale) || !isfinite(v_scale))
+        return RD_ERR_INVALID_ARG;
+    if (D != 128) return RD_ERR_UNSUPPORTED;
+    if (P_max > RD_MAX_PACKED || B > 65535 || Hkv > 65535) return RD_ERR_UNSUPPORTED;
+    if (mask_words != (P_max + 31) / 32) return RD_ERR_INVALID_ARG;
+    if (B == 0) return RD_OK;
+    if (total_ctx < 1) return RD_ERR_UNSUPPORTED;   /* no context: use rd_tree_attention */
+    if (!q || !k_new || !v_new || !k_cache || !v_cache || !ctx_offsets || !packed_len || !mask ||
+        !o)
+        return RD_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
+        !aligned16(v_cache) || !aligned16(o) || !aligned16(workspace))
+        return RD_ERR_INVALID_ARG;
+    const rd_attn_plan plan = rd_attn_make_plan(false, B, P_max, Hq, Hkv, D, max_ctx);
+    if (plan.ws_bytes > 0 && (!workspace || ws_bytes < plan.ws_bytes))
+        return RD_ERR_INVALID_ARG;
+    if (scale <= 0.f) scale = 1.0f / sqrtf((float)D);
+    rd_fp8_kv f8;
+    f8.k_cache = k_cache;
+    f8.v_cache = v_cache;
+    f8.k_scale = k_scale;
+    f8.v_scale = v_scale;
+    return from_cuda(rd_launch_attention(false, plan, B, P_max, Hq, Hkv, D, scale, q, k_new,
+                                         v_new, nullptr, nullptr, ctx_offsets, total_ctx,
+                                         max_ctx, packed_len, mask, mask_words, o, workspace,
+                                         dev_status, (cudaStream_t)stream, nullptr, &f8));
+}
+
 rd_status rd_tree_attention_paged(int B, int P_max, int Hq, int Hkv, int D, float scale,
                                   const void* q, const void* k_new, const void* v_new,
                                   const void* k_pool, const void* v_pool, int num_pages,

@@ -51,6 +51,11 @@ struct rd_paged_kv {
     const int32_t* ctx_lens;      // [B]
     int max_pages, page_size, num_pages;
 };
+struct rd_fp8_kv {
+    const void* k_cache;          // e4m3 [total_ctx, Hkv, D]
+    const void* v_cache;
+    float k_scale, v_scale;
+};
 rd_attn_plan rd_attn_make_plan(bool causal, int B, int P_max, int Hq, int Hkv, int D,
                                int max_kv);
 cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, int P_max,
@@ -60,7 +65,8 @@ cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, in
                                 const int64_t* ctx_offsets, int64_t total_kv, int max_kv,
                                 const int32_t* lens, const uint32_t* mask, int mask_words,
                                 void* o, void* workspace, int32_t* dev_status,
-                                cudaStream_t stream, const rd_paged_kv* paged = nullptr);
+                                cudaStream_t stream, const rd_paged_kv* paged = nullptr,
+                                const rd_fp8_kv* fp8 = nullptr);
 
 cudaError_t rd_launch_commit(int B, int W, int L, int P_max, int Hkv, int D, const void* k_new,
                              const void* v_new, const int32_t* unpacker,

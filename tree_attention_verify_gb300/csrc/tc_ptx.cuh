@@ -187,4 +187,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
          | ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor of kind::f16 with f16 A/B and fp32 D.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major, bool b_mn_major)
+{
+    return (1u << 4)                       // D format: f32
+         | ((a_mn_major ? 1u : 0u) << 15)  // A, B format 0: f16
+         | ((b_mn_major ? 1u : 0u) << 16)
+         | ((uint32_t)(N >> 3) << 17)
+         | ((uint32_t)(M >> 4) << 24);
+}
+
 }  // namespace rdtc

@@ -318,3 +318,12 @@ def make_paged(k_cache: torch.Tensor, v_cache: torch.Tensor, ctx_lens, page_size
         off += C
     return dict(k_pool=k_pool, v_pool=v_pool, block_table=torch.from_numpy(table).to(dev),
                 ctx_lens=torch.from_numpy(lens.astype(np.int32)).to(dev), page_size=page_size)
+
+
+def make_fp8_cache(cache: torch.Tensor) -> tuple:
+    """Quantise a bf16 cache [rows, Hkv, D] to e4m3 with one scale per tensor
+    (amax / 448, the largest finite e4m3 value).  Returns (uint8 codes, scale)."""
+    amax = float(cache.float().abs().max()) if cache.numel() else 1.0
+    scale = max(amax, 1e-30) / 448.0
+    codes = (cache.float() / scale).to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
+    return codes, scale
