@@ -60,22 +60,23 @@ constexpr long long kWaitBudget = 4000000000LL;   // ~2 s of SM clock per wait
 
 template <int D, bool F8 = false> struct Cfg {
     static constexpr int kDB = D / 64;                  // 64-element (128-byte) column blocks
-    static constexpr int kStages = F8 ? 3 : (D == 128 ? 5 : 8);   // 16-bit ring
+    static constexpr int kStages = F8 ? 5 : (D == 128 ? 7 : 8);   // 16-bit ring
     static constexpr int kF8Stages = F8 ? 4 : 0;        // 8-bit ring (context chunks)
-    static constexpr int kQBytes = kM * D * 2;
-    static constexpr int kPBytes = kM * kN * 2;         // one probability buffer
     static constexpr int kKBytes = kN * D * 2;          // one K (or V) chunk
     static constexpr int kStageBytes = 2 * kKBytes;
     static constexpr int kF8Bytes = 2 * kN * D;         // one 8-bit K + V chunk
-    static constexpr int kQOff = 0;
-    static constexpr int kPOff = kQOff + kQBytes;
-    static constexpr int kStageOff = kPOff + 2 * kPBytes;
+    static constexpr int kStageOff = 0;
     static constexpr int kF8Off = kStageOff + kStages * kStageBytes;
     static constexpr int kBarOff = kF8Off + kF8Stages * kF8Bytes;
     static constexpr int kSmemBytes = kBarOff + 512 + 1024;   // + barriers + alignment slack
-    static constexpr uint32_t kTmemCols = 256;          // S: 2 x 64, O: D (<= 128)
-    static constexpr uint32_t kSCol = 0;
-    static constexpr uint32_t kOCol = 128;
+    // Tensor memory (32-bit columns x 128 lanes; lane = query row of the tile):
+    // S double buffer, O accumulator, Q and a double-buffered P as 16-bit pairs
+    // (the A operands of the two MMAs).
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kSCol = 0;                // 2 x kN
+    static constexpr uint32_t kOCol = 2 * kN;           // D (<= 128)
+    static constexpr uint32_t kQCol = kOCol + 128;      // D / 2
+    static constexpr uint32_t kPCol = kQCol + 64;       // 2 x kN / 2
 };
 
 struct TcArgs {
@@ -465,11 +466,9 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             // Shared-memory descriptors differ only in their start-address field
             // (bits 0-13, address >> 4): build each base once and add offsets,
             // which keeps the issuing thread's work per MMA to two additions.
-            const uint64_t q_desc = smem_desc(smem_addr(smem + C::kQOff), 16, 1024, kSwizzle128B);
             const uint64_t k_desc = smem_desc(smem_addr(smem + C::kStageOff), 16, 1024, kSwizzle128B);
             const uint64_t v_desc = smem_desc(smem_addr(smem + C::kStageOff + C::kKBytes), kN * 128,
                                               1024, kSwizzle128B);
-            const uint64_t p_desc = smem_desc(smem_addr(smem + C::kPOff), 16, 1024, kSwizzle128B);
             // S = Q K^T for chunk gs (D/16 K-steps) into TMEM tile gs & 1.
             auto issue_s = [&](uint32_t gs) {
                 const uint64_t kd = k_desc + (uint64_t)(((gs % C::kStages) * C::kStageBytes) >> 4);
@@ -477,19 +476,18 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t off = ((ks >> 2) * (kN * 128) + (ks & 3) * 32) >> 4;
-                    const uint32_t qoff = ((ks >> 2) * (kM * 128) + (ks & 3) * 32) >> 4;
-                    mma_bf16(d_tmem, q_desc + qoff, kd + off, idS, ks > 0);
+                    mma_tmem_a(d_tmem, tmem + C::kQCol + ks * 8, kd + off, idS, ks > 0);
                 }
                 mma_commit(&bar.s_full[gs & 1]);
             };
             // O += P V for chunk gp (4 K-steps of 16 positions).
             auto issue_pv = [&](uint32_t gp, bool first) {
                 const uint64_t vd = v_desc + (uint64_t)(((gp % C::kStages) * C::kStageBytes) >> 4);
-                const uint64_t pd = p_desc + (uint64_t)(((gp & 1) * C::kPBytes) >> 4);
+                const uint32_t pt = tmem + C::kPCol + (gp & 1) * (kN / 2);
 #pragma unroll
                 for (int kk = 0; kk < kN / 16; ++kk)
-                    mma_bf16(tmem + C::kOCol, pd + (uint64_t)((kk * 32) >> 4),
-                             vd + (uint64_t)((kk * 2048) >> 4), idPV, !(first && kk == 0));
+                    mma_tmem_a(tmem + C::kOCol, pt + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), idPV,
+                               !(first && kk == 0));
                 mma_commit(&bar.kv_empty[gp % C::kStages]);
                 mma_commit(&bar.pv_done);
             };
@@ -560,7 +558,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             const int n = geo.n_ctx + geo.n_draft;
             const bool valid = row < geo.n_rows;
             const int qpos = row / a.G;                    // node p (tree) / token t (causal)
-            // ---- queries -> shared memory (128-byte swizzle, K-major) ----------
+            // ---- queries -> tensor memory (this thread's lane, 16-bit pairs) -----
             {
                 const uint4* src = nullptr;
                 if (valid) {
@@ -568,17 +566,23 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                                                  : (size_t)geo.b * a.P_max + qpos;
                     src = reinterpret_cast<const uint4*>(a.q + (qrow * a.Hq + hq0 + row % a.G) * D);
                 }
-                unsigned char* qs = smem + C::kQOff;
 #pragma unroll
-                for (int c = 0; c < D / 8; ++c) {
-                    uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-                    if constexpr (F8) {
-                        v.x = bf16x2_to_f16x2(v.x, 1.f); v.y = bf16x2_to_f16x2(v.y, 1.f);
-                        v.z = bf16x2_to_f16x2(v.z, 1.f); v.w = bf16x2_to_f16x2(v.w, 1.f);
+                for (int half = 0; half < D / 64; ++half) {
+                    uint32_t qv[32];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        uint4 v = valid ? __ldg(src + half * 8 + c) : make_uint4(0, 0, 0, 0);
+                        if constexpr (F8) {
+                            v.x = bf16x2_to_f16x2(v.x, 1.f); v.y = bf16x2_to_f16x2(v.y, 1.f);
+                            v.z = bf16x2_to_f16x2(v.z, 1.f); v.w = bf16x2_to_f16x2(v.w, 1.f);
+                        }
+                        qv[c * 4 + 0] = v.x; qv[c * 4 + 1] = v.y;
+                        qv[c * 4 + 2] = v.z; qv[c * 4 + 3] = v.w;
                     }
-                    *reinterpret_cast<uint4*>(qs + (c >> 3) * (kM * 128) + sw128(t, c & 7)) = v;
+                    tmem_st32(tmem + lane_base + C::kQCol + half * 32, qv);
                 }
-                fence_proxy_async_smem();
+                tmem_st_wait();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar.q_full);
             }
@@ -656,8 +660,8 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                     m = m_new;
                 }
                 const float base = (m == -INFINITY) ? 0.f : m;
-                unsigned char* ps = smem + C::kPOff + sb * C::kPBytes;
                 float lsum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                uint32_t pv[32];
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8) {
                     float p[8];
@@ -666,16 +670,14 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                         p[e] = fast_exp2(fmaf(s[c8 * 8 + e], a.scale_log2, -base));
                         lsum[e] += p[e];
                     }
-                    uint4 v;
-                    v.x = pack16<F8>(p[0], p[1]);
-                    v.y = pack16<F8>(p[2], p[3]);
-                    v.z = pack16<F8>(p[4], p[5]);
-                    v.w = pack16<F8>(p[6], p[7]);
-                    *reinterpret_cast<uint4*>(ps + sw128(t, c8)) = v;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) pv[c8 * 4 + e] = pack16<F8>(p[2 * e], p[2 * e + 1]);
                 }
+                // P (16-bit) into this lane's half of the P buffer: PV's A operand
+                tmem_st32(tmem + lane_base + C::kPCol + sb * (kN / 2), pv);
                 l += ((lsum[0] + lsum[1]) + (lsum[2] + lsum[3])) +
                      ((lsum[4] + lsum[5]) + (lsum[6] + lsum[7]));
-                fence_proxy_async_smem();
+                tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar.p_full[sb]);
