@@ -59,12 +59,14 @@ def _load():
             lib.oracle_tree_attention_fp8.argtypes = [I, I, I, I, I, ctypes.c_double, P, P, P, P,
                                                       P, ctypes.c_double, ctypes.c_double, P, P,
                                                       P, I, P]
+            lib.oracle_sample_accept.argtypes = [P, P, I, I, I, ctypes.c_double, P, P, P, P, I,
+                                                 I, P, P, P, P, P, P, P]
             lib.oracle_e4m3_value.argtypes = [I]
             lib.oracle_e4m3_value.restype = ctypes.c_double
             for f in (lib.oracle_pack, lib.oracle_tree_attention,
                       lib.oracle_tree_attention_paged, lib.oracle_causal_attention,
                       lib.oracle_greedy_accept, lib.oracle_beam_search_step,
-                      lib.oracle_tree_attention_fp8):
+                      lib.oracle_tree_attention_fp8, lib.oracle_sample_accept):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -216,6 +218,33 @@ def oracle_causal_attention(q, k, v, cu_seqlens, scale: float = 0.0,
     if rc != 0:
         raise ValueError(f"oracle_causal_attention rejected the input (rc={rc})")
     return o
+
+
+def oracle_sample_accept(target, draft, temperature, beams, packer, unpacker, packed_len,
+                         u_accept, u_sample) -> dict:
+    """Stochastic verification by multi-step speculative sampling (see
+    oracle_sample_accept in rd_oracle.c).  target/draft logits [B,P,V] (uint16
+    bf16 bits), beams/unpacker [B,W,L], packer [B,P], u_accept float32 [B,P],
+    u_sample float32 [B,V].  Returns accept_len, best_beam, n_accepted,
+    out_tokens and margin (the smallest relative gap of a decision taken)."""
+    target = _c(target, np.uint16); draft = _c(draft, np.uint16)
+    beams = _c(beams, np.int32); packer = _c(packer, np.int32)
+    unpacker = _c(unpacker, np.int32); packed_len = _c(packed_len, np.int32)
+    u_accept = _c(u_accept, np.float32); u_sample = _c(u_sample, np.float32)
+    B, P, V = target.shape
+    W, L = beams.shape[1], beams.shape[2]
+    out = dict(accept_len=np.zeros((B, W), np.int32), best_beam=np.zeros(B, np.int32),
+               n_accepted=np.zeros(B, np.int32), out_tokens=np.zeros((B, L), np.int32),
+               margin=np.zeros(B, np.float64))
+    rc = _load().oracle_sample_accept(_ptr(target), _ptr(draft), B, P, V, float(temperature),
+                                      _ptr(beams), _ptr(packer), _ptr(unpacker),
+                                      _ptr(packed_len), W, L, _ptr(u_accept), _ptr(u_sample),
+                                      _ptr(out["accept_len"]), _ptr(out["best_beam"]),
+                                      _ptr(out["n_accepted"]), _ptr(out["out_tokens"]),
+                                      _ptr(out["margin"]))
+    if rc != 0:
+        raise ValueError(f"oracle_sample_accept rejected the input (rc={rc})")
+    return out
 
 
 def oracle_greedy_accept(logits, beams, unpacker, packed_len) -> dict:

@@ -37,6 +37,10 @@
  *                          longest accepted draft prefix per beam, best beam
  *                          (NVIDIA blog introduction: verify and accept the best
  *                          path before drafting; news page: greedy decoding).
+ *   oracle_sample_accept   stochastic verification of the draft tree by
+ *                          multi-step speculative sampling (speculative-decoding
+ *                          survey page: the rejection-sampling paragraph and
+ *                          SpecInfer's "Token Tree Verifier").
  *
  * Readings where the pages are silent (each also listed in the design notes):
  *  - position 0 of every beam is the anchor (already emitted by the LLM);
@@ -567,4 +571,144 @@ int oracle_tree_attention_fp8(int B, int P_max, int Hq, int Hkv, int D, double s
     }
     free(s_buf);
     return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* stochastic verification: multi-step speculative sampling over the tree    */
+/* ------------------------------------------------------------------------ */
+/*
+ * Rejection sampling (speculative-decoding survey page, rejection-sampling
+ * paragraph): a token x proposed by the draft distribution q is kept when
+ * u < p(x) / q(x), u ~ U(0,1), p the target distribution.  Multi-step
+ * speculative sampling (same page, SpecInfer "Token Tree Verifier"): the
+ * children of the current tree node are tested in turn; after each rejection
+ * the target becomes the normalised residual max(0, p - q); if every child is
+ * rejected, or the node has no child, one token is drawn from the current
+ * target and the walk ends.
+ *
+ * Readings (the pages leave these open):
+ *  - p(.|n) = softmax(target_logits[n] / T), q(.|n) = softmax(draft_logits[n] / T):
+ *    the LLM's and the drafter's next-token distributions after node n;
+ *  - the walk starts at packed node 0 (beam 0's anchor); the children of node
+ *    n are the packed nodes whose parent is n, tested in increasing packed
+ *    index; the test u * q(x) < p(x) is the ratio test without the division;
+ *  - a residual whose mass is 0 leaves the target unchanged;
+ *  - a draw from a distribution R is the exponential race
+ *    argmin_y E_y / R(y) with E_y = -ln(u_sample[b][y]) (lowest y on ties),
+ *    which draws y with probability R(y) / sum R;
+ *  - the emitted tokens are the accepted drafts and the drawn token;
+ *    best_beam is the lowest beam whose prefix is the accepted walk;
+ *    accept_len[w] is how many of beam w's leading drafts lie on the walk.
+ * margin[b] (optional) returns the smallest relative gap of any decision taken
+ * for request b (the two sides of a ratio test; the best and second-best race
+ * keys), so that callers can tell a well-conditioned decision from a tie.
+ */
+static void softmax_row(const uint16_t* row, int V, double inv_T, double* out)
+{
+    double mx = -INFINITY, sum = 0.0;
+    for (int v = 0; v < V; ++v) {
+        double x = bf16_to_f64(row[v]) * inv_T;
+        if (x > mx) mx = x;
+    }
+    for (int v = 0; v < V; ++v) {
+        out[v] = exp(bf16_to_f64(row[v]) * inv_T - mx);
+        sum += out[v];
+    }
+    for (int v = 0; v < V; ++v) out[v] /= sum;
+}
+
+static double rel_gap(double a, double b)
+{
+    double m = fabs(a) > fabs(b) ? fabs(a) : fabs(b);
+    return m > 0.0 ? fabs(a - b) / m : 0.0;
+}
+
+int oracle_sample_accept(const uint16_t* target, const uint16_t* draft, int B, int P_max, int V,
+                         double temperature, const int32_t* beams, const int32_t* packer,
+                         const int32_t* unpacker, const int32_t* packed_len, int W, int L,
+                         const float* u_accept, const float* u_sample, int32_t* accept_len,
+                         int32_t* best_beam, int32_t* n_accepted, int32_t* out_tokens,
+                         double* margin)
+{
+    if (B < 0 || P_max <= 0 || V <= 0 || W <= 0 || L <= 0 || !(temperature > 0.0)) return -1;
+    const double inv_T = 1.0 / temperature;
+    double* p = (double*)malloc(sizeof(double) * V);
+    double* q = (double*)malloc(sizeof(double) * V);
+    int32_t* walk = (int32_t*)malloc(sizeof(int32_t) * L);
+    if (!p || !q || !walk) { free(p); free(q); free(walk); return -2; }
+    int rc = 0;
+    for (int b = 0; b < B && rc == 0; ++b) {
+        const int Pb = packed_len[b];
+        if (Pb < 1 || Pb > P_max) { rc = -1; break; }
+        const int32_t* bb = beams + (size_t)b * W * L;
+        const int32_t* pk = packer + (size_t)b * P_max;
+        const int32_t* up = unpacker + (size_t)b * W * L;
+        double worst = 1.0;
+        int node = 0, a = 0;
+        walk[0] = 0;
+        for (;;) {
+            const uint16_t* trow = target + ((size_t)b * P_max + node) * V;
+            const uint16_t* drow = draft + ((size_t)b * P_max + node) * V;
+            softmax_row(trow, V, inv_T, p);          /* p: the current target */
+            softmax_row(drow, V, inv_T, q);
+            int accepted = -1;
+            for (int c = node + 1; c < Pb && accepted < 0; ++c) {
+                const int f = pk[c], w = f / L, i = f % L;
+                if (i == 0 || up[w * L + i - 1] != node) continue;   /* not a child */
+                const int x = bb[w * L + i];
+                if (x < 0 || x >= V) { rc = -1; break; }
+                const double lhs = (double)u_accept[(size_t)b * P_max + c] * q[x];
+                const double g = rel_gap(lhs, p[x]);
+                if (g < worst) worst = g;
+                if (lhs < p[x]) {
+                    accepted = c;
+                } else {                              /* residual max(0, p - q) */
+                    double Z = 0.0;
+                    for (int v = 0; v < V; ++v) Z += (p[v] > q[v] ? p[v] - q[v] : 0.0);
+                    if (Z > 0.0)
+                        for (int v = 0; v < V; ++v) p[v] = (p[v] > q[v] ? p[v] - q[v] : 0.0) / Z;
+                }
+            }
+            if (rc) break;
+            if (accepted >= 0) {
+                const int f = pk[accepted];
+                out_tokens[(size_t)b * L + a] = bb[f];
+                ++a;
+                walk[a] = accepted;
+                node = accepted;
+                continue;
+            }
+            /* draw one token from p: the exponential race */
+            const float* us = u_sample + (size_t)b * V;
+            double k1 = INFINITY, k2 = INFINITY;
+            int y1 = -1;
+            for (int v = 0; v < V; ++v) {
+                if (!(p[v] > 0.0)) continue;
+                const double key = -log((double)us[v]) / p[v];
+                if (key < k1) { k2 = k1; k1 = key; y1 = v; }
+                else if (key < k2) k2 = key;
+            }
+            if (y1 < 0) { rc = -1; break; }
+            if (isfinite(k2)) {
+                const double g = (k2 - k1) / k2;
+                if (g < worst) worst = g;
+            }
+            out_tokens[(size_t)b * L + a] = y1;
+            break;
+        }
+        if (rc) break;
+        for (int j = a + 1; j < L; ++j) out_tokens[(size_t)b * L + j] = -1;
+        n_accepted[b] = a;
+        int best = -1;
+        for (int w = 0; w < W; ++w) {
+            int n = -1;
+            while (n + 1 <= a && up[w * L + n + 1] == walk[n + 1]) ++n;
+            accept_len[(size_t)b * W + w] = n < 0 ? 0 : n;
+            if (n == a && best < 0) best = w;
+        }
+        best_beam[b] = best;
+        if (margin) margin[b] = worst;
+    }
+    free(p); free(q); free(walk);
+    return rc;
 }
