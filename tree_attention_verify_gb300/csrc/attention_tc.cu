@@ -587,6 +587,9 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 if (lane == 0) mbar_arrive(&bar.q_full);
             }
             float m = -INFINITY, l = 0.f;
+            // a warp whose 32 rows are all padding reads no scores: it keeps the
+            // barrier protocol and zeroes its P rows once per buffer and unit
+            const bool dead = __all_sync(0xffffffffu, !valid);
             const uint32_t* mrow = (!a.causal && valid)
                 ? a.mask + ((size_t)geo.b * a.P_max + qpos) * a.mask_words : nullptr;
             bool ok = true;
@@ -595,6 +598,21 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 const int sb = gg & 1;
                 if (!warp_wait(&bar.s_full[sb], (gg >> 1) & 1, abort, kWaitBudget)) { ok = false; break; }
                 tc_fence_after();
+                if (dead) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar.s_free[sb]);
+                    if (j < 2) {
+                        uint32_t zero[32];
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) zero[c] = 0u;
+                        tmem_st32(tmem + lane_base + C::kPCol + sb * (kN / 2), zero);
+                        tmem_st_wait();
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar.p_full[sb]);
+                    continue;
+                }
                 uint32_t sr[64];
                 tmem_ld32(tmem + lane_base + C::kSCol + sb * kN, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
                 tmem_ld32(tmem + lane_base + C::kSCol + sb * kN + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
