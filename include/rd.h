@@ -356,6 +356,48 @@ rd_status rd_greedy_accept_noalloc(const void* logits, int B, int P_max, int V,
                                    int32_t* out_tokens, int32_t* dev_status,
                                    rd_stream_t stream);
 
+/*
+ * rd_sample_accept -- stochastic verification of the draft tree by multi-step
+ * speculative sampling: rejection sampling (speculative-decoding survey page,
+ * rejection-sampling paragraph: keep a proposal x when u < p(x) / q(x)) applied
+ * child by child over the tree as in SpecInfer's multi-step speculative
+ * sampling (same page, "Token Tree Verifier").
+ *
+ * For request b the walk starts at packed node 0 (beam 0's anchor).  At node n,
+ * with p = softmax(target_logits[b, n] / temperature) and
+ * q = softmax(draft_logits[b, n] / temperature), the children of n (the packed
+ * nodes whose parent is n) are tested in increasing packed index: child c with
+ * token x is accepted when u_accept[b, c] * q(x) < p(x) and becomes the current
+ * node; after a rejection p is replaced by max(0, p - q) / sum(max(0, p - q))
+ * (left unchanged when that sum is 0).  When every child is rejected, or n has
+ * none, one token is drawn from p by the exponential race
+ * argmin_y -ln(u_sample[b, y]) / p(y) (lowest y on ties) and the walk ends.
+ *
+ * target_logits, draft_logits  bf16 [B, P_max, V]: the LLM's and the drafter's
+ *                 next-token logits at every packed node
+ * beams, unpacker int32 [B, W, L]; packer int32 [B, P_max]; packed_len int32 [B]
+ *                 (as produced by rd_pack_beams)
+ * temperature     finite, > 0
+ * u_accept        float32 [B, P_max] uniforms in [0, 1), one per packed node
+ * u_sample        float32 [B, V] uniforms in [0, 1), one per vocabulary entry
+ * accept_len      int32 [B, W] out: leading drafts of beam w on the accepted walk
+ * best_beam       int32 [B] out: lowest beam whose prefix is the accepted walk
+ * n_accepted      int32 [B] out: accepted drafts a
+ * out_tokens      int32 [B, L] out: the a accepted drafts, the drawn token, then -1
+ * Computes in fp32 (decisions closer than fp32 rounding may differ from exact
+ * arithmetic).  Supported: W <= 32, P_max <= 256 (RD_ERR_UNSUPPORTED).  Device
+ * errors: packed_len outside [1, P_max] sets RD_DEV_BAD_LENGTH (outputs 0 / -1);
+ * a packer or parent index out of range RD_DEV_BAD_INDEX and a token outside
+ * [0, V) RD_DEV_BAD_TOKEN (that node is never accepted).  No workspace.
+ */
+rd_status rd_sample_accept(const void* target_logits, const void* draft_logits, int B, int P_max,
+                           int V, float temperature, const int32_t* beams,
+                           const int32_t* packer, const int32_t* unpacker,
+                           const int32_t* packed_len, int W, int L, const float* u_accept,
+                           const float* u_sample, int32_t* accept_len, int32_t* best_beam,
+                           int32_t* n_accepted, int32_t* out_tokens, int32_t* dev_status,
+                           rd_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

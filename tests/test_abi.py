@@ -90,3 +90,22 @@ def test_product_path_has_no_oracle_dependency():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in text.lower().replace("oracles", ""), f
+
+
+def test_sample_accept_host_validation():
+    import tree_attention_verify_gb300 as rd
+    lib = rd._lib
+    N = None
+    # empty batch: OK without a device; bad temperature; too many beams / packed nodes
+    assert lib.rd_sample_accept(N, N, 0, 48, 32000, 1.0, N, N, N, N, 8, 6, N, N, N, N, N, N, N,
+                                N) == rd.RD_OK
+    for T in (0.0, -1.0, float("inf"), float("nan")):
+        assert lib.rd_sample_accept(N, N, 1, 48, 32000, T, N, N, N, N, 8, 6, N, N, N, N, N, N,
+                                    N, N) == rd.RD_ERR_INVALID_ARG
+    assert lib.rd_sample_accept(N, N, 1, 48, 32000, 1.0, N, N, N, N, 33, 6, N, N, N, N, N, N, N,
+                                N) == rd.RD_ERR_UNSUPPORTED
+    assert lib.rd_sample_accept(N, N, 1, 300, 32000, 1.0, N, N, N, N, 8, 6, N, N, N, N, N, N, N,
+                                N) == rd.RD_ERR_UNSUPPORTED
+    # null pointers with a non-empty batch
+    assert lib.rd_sample_accept(N, N, 1, 48, 32000, 1.0, N, N, N, N, 8, 6, N, N, N, N, N, N, N,
+                                N) == rd.RD_ERR_INVALID_ARG

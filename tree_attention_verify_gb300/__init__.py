@@ -63,6 +63,7 @@ def _load() -> ctypes.CDLL:
         "rd_beam_search_step": [P, P, P, I, I, I, I, P, P, P, P, P],
         "rd_tree_attention_fp8": [I, I, I, I, I, F, P, P, P, P, P, F, F, P, I64, I, P, P, I, P, P,
                                   S, P, P],
+        "rd_sample_accept": [P, P, I, I, I, F, P, P, P, P, I, I, P, P, P, P, P, P, P, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -346,6 +347,39 @@ def rd_greedy_accept(logits, beams, unpacker, packed_len, *, out=None, workspace
         _ptr(out["argmax"]), _ptr(out["accept_len"]), _ptr(out["best_beam"]),
         _ptr(out["n_accepted"]), _ptr(out["out_tokens"]), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream)))
+    return out
+
+
+def rd_sample_accept(target_logits, draft_logits, temperature: float, beams, packer, unpacker,
+                     packed_len, u_accept, u_sample, *, out=None, dev_status=None,
+                     stream=None) -> dict:
+    """Stochastic verification by multi-step speculative sampling (see
+    rd_sample_accept in rd.h).  Returns dict(accept_len, best_beam, n_accepted,
+    out_tokens)."""
+    _need(target_logits, "target_logits", torch.bfloat16, ndim=3)
+    _need(draft_logits, "draft_logits", torch.bfloat16, ndim=3)
+    _need(beams, "beams", torch.int32, ndim=3)
+    _need(packer, "packer", torch.int32, ndim=2)
+    _need(unpacker, "unpacker", torch.int32, ndim=3)
+    _need(packed_len, "packed_len", torch.int32, ndim=1)
+    _need(u_accept, "u_accept", torch.float32, ndim=2)
+    _need(u_sample, "u_sample", torch.float32, ndim=2)
+    B, P, V = target_logits.shape
+    _, W, L = beams.shape
+    if draft_logits.shape != target_logits.shape or packer.shape != (B, P):
+        raise ValueError("draft_logits / packer shapes do not match target_logits")
+    if u_accept.shape != (B, P) or u_sample.shape != (B, V):
+        raise ValueError("u_accept must be [B, P_max] and u_sample [B, V]")
+    if out is None:
+        out = dict(accept_len=_empty((B, W), torch.int32, target_logits),
+                   best_beam=_empty((B,), torch.int32, target_logits),
+                   n_accepted=_empty((B,), torch.int32, target_logits),
+                   out_tokens=_empty((B, L), torch.int32, target_logits))
+    _check("rd_sample_accept", _lib.rd_sample_accept(
+        _ptr(target_logits), _ptr(draft_logits), B, P, V, float(temperature), _ptr(beams),
+        _ptr(packer), _ptr(unpacker), _ptr(packed_len), W, L, _ptr(u_accept), _ptr(u_sample),
+        _ptr(out["accept_len"]), _ptr(out["best_beam"]), _ptr(out["n_accepted"]),
+        _ptr(out["out_tokens"]), _ptr(dev_status), _stream(stream)))
     return out
 
 

@@ -252,6 +252,29 @@ rd_status rd_greedy_accept(const void* logits, int B, int P_max, int V,
                                              (cudaStream_t)stream));
 }
 
+rd_status rd_sample_accept(const void* target_logits, const void* draft_logits, int B, int P_max,
+                           int V, float temperature, const int32_t* beams,
+                           const int32_t* packer, const int32_t* unpacker,
+                           const int32_t* packed_len, int W, int L, const float* u_accept,
+                           const float* u_sample, int32_t* accept_len, int32_t* best_beam,
+                           int32_t* n_accepted, int32_t* out_tokens, int32_t* dev_status,
+                           rd_stream_t stream)
+{
+    if (B < 0 || P_max < 1 || V < 1 || W < 1 || L < 1) return RD_ERR_INVALID_ARG;
+    if (!(temperature > 0.f) || !isfinite(temperature)) return RD_ERR_INVALID_ARG;
+    if (W > RD_MAX_BEAMS || P_max > RD_MAX_PACKED || L > RD_MAX_PACKED || B > 0x7fffffff)
+        return RD_ERR_UNSUPPORTED;
+    if (B == 0) return RD_OK;
+    if (!target_logits || !draft_logits || !beams || !packer || !unpacker || !packed_len ||
+        !u_accept || !u_sample || !accept_len || !best_beam || !n_accepted || !out_tokens)
+        return RD_ERR_INVALID_ARG;
+    return from_cuda(rd_launch_sample_accept(target_logits, draft_logits, B, P_max, V,
+                                             temperature, beams, packer, unpacker, packed_len,
+                                             W, L, u_accept, u_sample, accept_len, best_beam,
+                                             n_accepted, out_tokens, dev_status,
+                                             (cudaStream_t)stream));
+}
+
 rd_status rd_beam_search_step(const void* logits, const float* scores_in,
                               const int32_t* beams_in, int B, int W, int V, int t,
                               int32_t* beams_out, float* scores_out, int32_t* parent,

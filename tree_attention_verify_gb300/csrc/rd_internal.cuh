@@ -39,6 +39,15 @@ cudaError_t rd_launch_greedy_accept(const void* logits, int B, int P_max, int V,
                                     int32_t* out_tokens, void* workspace,
                                     int32_t* dev_status, cudaStream_t stream);
 
+cudaError_t rd_launch_sample_accept(const void* target, const void* draft, int B, int P_max,
+                                    int V, float temperature, const int32_t* beams,
+                                    const int32_t* packer, const int32_t* unpacker,
+                                    const int32_t* packed_len, int W, int L,
+                                    const float* u_accept, const float* u_sample,
+                                    int32_t* accept_len, int32_t* best_beam,
+                                    int32_t* n_accepted, int32_t* out_tokens,
+                                    int32_t* dev_status, cudaStream_t stream);
+
 // Attention (tree and causal modes share one kernel family).
 struct rd_attn_plan {
     int tiles;         // row tiles per (request, kv head)

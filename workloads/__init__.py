@@ -327,3 +327,35 @@ def make_fp8_cache(cache: torch.Tensor) -> tuple:
     scale = max(amax, 1e-30) / 448.0
     codes = (cache.float() / scale).to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
     return codes, scale
+
+
+def make_draft_logits(target: torch.Tensor, gen: torch.Generator, mix: float = 0.7,
+                      noise: float = 1.0) -> torch.Tensor:
+    """Drafter logits correlated with the target's: bf16(mix * target + N(0, noise))."""
+    n = torch.randn(target.shape, generator=gen, device=target.device, dtype=torch.float32)
+    return (mix * target.float() + noise * n).to(torch.bfloat16)
+
+
+def make_uniforms(B: int, P_max: int, V: int, rng: np.random.Generator) -> tuple:
+    """The random numbers of stochastic verification: u_accept [B, P_max] and
+    u_sample [B, V], float32 uniforms in [0, 1)."""
+    return (torch.from_numpy(rng.random((B, P_max), dtype=np.float32)),
+            torch.from_numpy(rng.random((B, V), dtype=np.float32)))
+
+
+def make_sample_inputs(cfg: GenConfig, temperature: float = 1.0, device="cpu",
+                       seed: Optional[int] = None) -> dict:
+    """Inputs of stochastic verification for a generation sub-batch: beams, target
+    logits (as make_logits), drafter logits correlated with them, and uniforms."""
+    seed = cfg.seed if seed is None else seed
+    rng = np.random.default_rng(seed + 1000)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed + 1000)
+    trees = draft_trees(cfg.B, cfg.W, cfg.L, cfg.vocab, cfg.share, rng)
+    target = make_logits(trees, cfg.P_max, cfg.vocab, cfg.plant, rng, gen, device,
+                         ties=cfg.ties)
+    draft = make_draft_logits(target, gen)
+    u_accept, u_sample = make_uniforms(cfg.B, cfg.P_max, cfg.vocab, rng)
+    return dict(cfg=cfg, temperature=temperature, trees=trees,
+                beams=torch.from_numpy(trees.beams.copy()).to(device), target=target,
+                draft=draft, u_accept=u_accept.to(device), u_sample=u_sample.to(device))
