@@ -49,11 +49,12 @@ using namespace rdtc;
 constexpr int kM = 128;                    // query rows per tile = TMEM lanes
 constexpr int kN = 64;                     // KV positions per chunk
 constexpr int kSoftmaxThreads = 128;
-constexpr int kThreads = kSoftmaxThreads + 64;
-constexpr int kThreadsF8 = kThreads + 128;   // + four converter warps
+constexpr int kThreads = kSoftmaxThreads + 96;          // + producer, S issuer, PV issuer
+constexpr int kThreadsF8 = kSoftmaxThreads + 64 + 128;  // + producer, MMA issuer, 4 converters
 constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kConvWarp0 = 6;
+constexpr int kMmaWarp = 5;                // bf16: S issuer; FP8: S and PV issuer
+constexpr int kPvWarp = 6;                 // bf16 only: PV issuer
+constexpr int kConvWarp0 = 6;              // FP8 only: first converter warp
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when a max grows by > 2^8
 constexpr long long kWaitBudget = 4000000000LL;   // ~2 s of SM clock per wait
@@ -113,6 +114,7 @@ struct Barriers {
     uint64_t s_free[2];
     uint64_t p_full[2];
     uint64_t pv_done;
+    uint64_t p_free[2];
     uint64_t o_final;
     uint64_t q_full;
     uint64_t drain;
@@ -274,7 +276,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
     if (tid == 0) {
         for (int i = 0; i < C::kStages; ++i) {
             mbar_init(&bar.kv_full[i], F8 ? 4 : 1);        // F8: the four converter warps
-            mbar_init(&bar.kv_empty[i], 1);
+            mbar_init(&bar.kv_empty[i], F8 ? 1 : 2);       // bf16: K read by S, V read by PV
         }
         for (int i = 0; i < C::kF8Stages; ++i) {
             mbar_init(&bar.f8_full[i], 1);
@@ -288,7 +290,9 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
         mbar_init(&bar.pv_done, 1);
         mbar_init(&bar.o_final, 1);
         mbar_init(&bar.q_full, 4);
-        mbar_init(&bar.drain, 1);
+        mbar_init(&bar.drain, F8 ? 1 : 2);
+        mbar_init(&bar.p_free[0], 1);
+        mbar_init(&bar.p_free[1], 1);
         bar.abort = 0;
         mbar_fence_init();
     }
@@ -458,7 +462,9 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 mbar_wait(&bar.kv_full[k % C::kStages], (k / C::kStages) & 1, &no_abort, kWaitBudget);
         }
     } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------ MMA issuer
+        // bf16: S = Q K^T only (the PV issuer runs in its own warp, so the two
+        // chains overlap); FP8: S and O += P V from this one thread.
         if (lane == 0) {
             constexpr uint32_t idS = F8 ? idesc_f16(kM, kN, false, false) : idesc_bf16(kM, kN, false, false);
             constexpr uint32_t idPV = F8 ? idesc_f16(kM, D, false, true) : idesc_bf16(kM, D, false, true);
@@ -498,8 +504,8 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 if (!mbar_wait(&bar.q_full, unit_iter & 1, abort, kWaitBudget)) { fail(); break; }
                 tc_fence_after();
                 bool ok = true;
-                // S_j as soon as chunk j has landed and its TMEM tile is free, then
-                // PV_{j-1} once the softmax has written P_{j-1}.
+                // S_j as soon as chunk j has landed and its TMEM tile is free; FP8:
+                // then PV_{j-1} once the softmax has written P_{j-1}.
                 for (int j = 0; j < n && ok; ++j) {
                     const uint32_t gg = g + j;
                     if (!mbar_wait(&bar.kv_full[gg % C::kStages], (gg / C::kStages) & 1, abort, kWaitBudget) ||
@@ -509,7 +515,9 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                     }
                     tc_fence_after();
                     issue_s(gg);
-                    if (j >= 1) {
+                    if constexpr (!F8) {
+                        mma_commit(&bar.kv_empty[gg % C::kStages]);     // K of the stage read
+                    } else if (j >= 1) {
                         if (!mbar_wait(&bar.p_full[(gg - 1) & 1], ((gg - 1) >> 1) & 1, abort, kWaitBudget)) {
                             ok = false;
                             break;
@@ -518,20 +526,60 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                         issue_pv(gg - 1, j == 1);
                     }
                 }
-                if (ok) {
-                    const uint32_t gl = g + n - 1;
-                    if (!mbar_wait(&bar.p_full[gl & 1], (gl >> 1) & 1, abort, kWaitBudget)) ok = false;
-                    else {
-                        tc_fence_after();
-                        issue_pv(gl, n == 1);
+                if constexpr (F8) {
+                    if (ok) {
+                        const uint32_t gl = g + n - 1;
+                        if (!mbar_wait(&bar.p_full[gl & 1], (gl >> 1) & 1, abort, kWaitBudget)) ok = false;
+                        else {
+                            tc_fence_after();
+                            issue_pv(gl, n == 1);
+                        }
                     }
                 }
                 if (!ok) { fail(); break; }
-                mma_commit(&bar.o_final);
+                if constexpr (F8) mma_commit(&bar.o_final);
                 g += n;
                 ++unit_iter;
             }
             // drain: every issued MMA must finish before TMEM is freed
+            mma_commit(&bar.drain);
+            mbar_wait(&bar.drain, 0, &no_abort, kWaitBudget);
+        }
+    } else if (!F8 && warp == kPvWarp) {
+        // ------------------------------------------------------- PV issuer (bf16)
+        // O += P V for every chunk once the softmax has written its P; the P
+        // buffer is released per buffer (p_free) and the stage's V read is the
+        // second arrival on kv_empty.
+        if (lane == 0) {
+            constexpr uint32_t idPV = idesc_bf16(kM, D, false, true);
+            uint32_t g = 0;
+            const uint64_t v_desc = smem_desc(smem_addr(smem + C::kStageOff + C::kKBytes), kN * 128,
+                                              1024, kSwizzle128B);
+            for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
+                const UnitGeo geo = unit_geo(a, u);
+                if (!geo.live) continue;
+                const int n = geo.n_ctx + geo.n_draft;
+                bool ok = true;
+                for (int j = 0; j < n; ++j) {
+                    const uint32_t gg = g + j;
+                    if (!mbar_wait(&bar.p_full[gg & 1], (gg >> 1) & 1, abort, kWaitBudget)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t vd = v_desc + (uint64_t)(((gg % C::kStages) * C::kStageBytes) >> 4);
+                    const uint32_t pt = tmem + C::kPCol + (gg & 1) * (kN / 2);
+#pragma unroll
+                    for (int kk = 0; kk < kN / 16; ++kk)
+                        mma_tmem_a(tmem + C::kOCol, pt + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), idPV,
+                                   !(j == 0 && kk == 0));
+                    mma_commit(&bar.kv_empty[gg % C::kStages]);
+                    mma_commit(&bar.p_free[gg & 1]);
+                }
+                if (!ok) { fail(); break; }
+                mma_commit(&bar.o_final);
+                g += n;
+            }
             mma_commit(&bar.drain);
             mbar_wait(&bar.drain, 0, &no_abort, kWaitBudget);
         }
@@ -601,6 +649,15 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 if (dead) {
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bar.s_free[sb]);
+                    // bf16: like the live warps, arrive for chunk gg only once PV of
+                    // chunk gg-2 has released the buffer, so that no arrival runs
+                    // ahead into an earlier phase of p_full
+                    if (!F8 && gg >= 2 &&
+                        !warp_wait(&bar.p_free[sb], ((gg >> 1) - 1) & 1, abort, kWaitBudget)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
                     if (j < 2) {
                         uint32_t zero[32];
 #pragma unroll
@@ -659,7 +716,12 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 const float m_new = need ? ms : m;
                 if (__any_sync(0xffffffffu, need) && j > 0) {
                     // O holds earlier chunks: wait for PV of the previous chunk, then rescale
-                    if (!warp_wait(&bar.pv_done, (gg - 1) & 1, abort, kWaitBudget)) { ok = false; break; }
+                    // (bf16: PV_{j-1} is done when it has released its P buffer; a
+                    // per-buffer barrier cannot lag two phases behind the wait)
+                    const bool pv_prev = F8 ? warp_wait(&bar.pv_done, (gg - 1) & 1, abort, kWaitBudget)
+                                            : warp_wait(&bar.p_free[(gg - 1) & 1], ((gg - 1) >> 1) & 1,
+                                                        abort, kWaitBudget);
+                    if (!pv_prev) { ok = false; break; }
                     tc_fence_after();
                     const float alpha = need ? fast_exp2(m - m_new) : 1.f;
 #pragma unroll
@@ -692,6 +754,14 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                     for (int e = 0; e < 4; ++e) pv[c8 * 4 + e] = pack16<F8>(p[2 * e], p[2 * e + 1]);
                 }
                 // P (16-bit) into this lane's half of the P buffer: PV's A operand
+                // (bf16: once PV of the chunk two back has released that buffer;
+                // FP8: S_j was issued after PV_{j-2}, so that is already true)
+                if (!F8 && gg >= 2 &&
+                    !warp_wait(&bar.p_free[sb], ((gg >> 1) - 1) & 1, abort, kWaitBudget)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
                 tmem_st32(tmem + lane_base + C::kPCol + sb * (kN / 2), pv);
                 l += ((lsum[0] + lsum[1]) + (lsum[2] + lsum[3])) +
                      ((lsum[4] + lsum[5]) + (lsum[6] + lsum[7]));
