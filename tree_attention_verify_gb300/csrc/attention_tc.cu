@@ -11,26 +11,29 @@
 // Work unit = (request b, kv head h, 128-row query tile, KV split).  The G query
 // heads that share kv head h are stacked as rows (row r -> node p = r / G, head
 // h*G + r % G; causal: token t = r / G), so each K/V byte is read once per tile.
-// Row r of a tile is TMEM lane r.  A unit walks its KV chunks of 64 positions:
-// first the context (all visible; the last chunk is ragged), then the packed
-// drafts (visible iff the node's ancestor-mask bit is set).
+// Row r of a tile is TMEM lane r.  A unit walks its KV chunks (64 positions;
+// FP8: 128): first the context (all visible; the last chunk is ragged), then
+// the packed drafts (visible iff the node's ancestor-mask bit is set).
 //
-// Warp roles (192 threads, one CTA per SM, persistent over units):
-//   warps 0-3  softmax: TMEM lane = row.  Load the tile's queries into shared
-//              memory, turn S into bf16 probabilities P (online softmax in exp2
-//              form, rescaling O in TMEM only when a row maximum grows by more
-//              than 2^8), and write the output rows.
+// Warp roles (one CTA per SM, persistent over units):
+//   warps 0-3  softmax: TMEM lane = row.  Write the tile's queries into TMEM,
+//              turn S into 16-bit probabilities P in TMEM (online softmax in
+//              exp2 form, rescaling O in TMEM only when a row maximum grows by
+//              more than 2^8), and write the output rows.
 //   warp 4     producer: TMA loads of K and V chunks (128-byte swizzle) into a
 //              ring of stages.
-//   warp 5     MMA issuer: S = Q K^T (M=128, N=64, K=D) into a double-buffered
-//              TMEM tile, then O += P V (M=128, N=D, K=64) into TMEM.
+//   warp 5     S issuer: S = Q K^T (M=128, N=chunk, K=D; A = Q in TMEM) into a
+//              double-buffered TMEM tile.
+//   warp 6     PV issuer: O += P V (M=128, N=D, K=chunk; A = P in TMEM) into
+//              TMEM.  The two issuers run independently.
 // FP8 variant (template flag F8; context K/V stored as e4m3 with per-tensor
-// scales): the producer TMA-loads e4m3 context chunks into an 8-bit ring; four
-// more warps (6-9) widen them (exactly) into the 16-bit ring the MMA reads, and
-// convert the bf16 draft chunks, divided by the scales, the same way.  The MMA
-// then runs kind::f16 with f16 operands (e4m3 widens to f16 exactly and both
-// operands of one MMA share a type); the K scale is folded into the softmax
-// scale and the V scale into the output normalisation.
+// scales): 128-position chunks; the producer TMA-loads e4m3 context chunks
+// into an 8-bit ring; warps 6-9 widen them (exactly) into the 16-bit ring the
+// MMA reads, and convert the bf16 draft chunks, divided by the scales, the same
+// way; warp 5 issues both S and PV; P is written over the first half of its
+// chunk's S buffer.  The MMA runs kind::f16 with f16 operands (e4m3 widens to
+// f16 exactly and both operands of one MMA share a type); the K scale is
+// folded into the softmax scale and the V scale into the output normalisation.
 // Every wait is bounded by a clock budget; on expiry the CTA records
 // RD_DEV_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
@@ -47,7 +50,8 @@ namespace {
 using namespace rdtc;
 
 constexpr int kM = 128;                    // query rows per tile = TMEM lanes
-constexpr int kN = 64;                     // KV positions per chunk
+constexpr int kN = 64;                     // KV positions per chunk (bf16)
+constexpr int kNF8 = 64;                   // KV positions per chunk (FP8)
 constexpr int kSoftmaxThreads = 128;
 constexpr int kThreads = kSoftmaxThreads + 96;          // + producer, S issuer, PV issuer
 constexpr int kThreadsF8 = kSoftmaxThreads + 64 + 128;  // + producer, MMA issuer, 4 converters
@@ -60,24 +64,39 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when a max g
 constexpr long long kWaitBudget = 4000000000LL;   // ~2 s of SM clock per wait
 
 template <int D, bool F8 = false> struct Cfg {
+    static constexpr int kNc = F8 ? kNF8 : kN;         // KV positions per chunk
     static constexpr int kDB = D / 64;                  // 64-element (128-byte) column blocks
-    static constexpr int kStages = F8 ? 5 : (D == 128 ? 7 : 8);   // 16-bit ring
-    static constexpr int kF8Stages = F8 ? 4 : 0;        // 8-bit ring (context chunks)
-    static constexpr int kKBytes = kN * D * 2;          // one K (or V) chunk
+    // 16-bit ring and (FP8) 8-bit ring of context chunks, 224 KB in all
+    static constexpr int kStages = F8 ? (kNc == 128 ? 2 : 5) : (D == 128 ? 7 : 8);
+    static constexpr int kF8Stages = F8 ? (kNc == 128 ? 3 : 4) : 0;
+    static constexpr int kF8Ring = kF8Stages > 0 ? kF8Stages : 1;   // ring index modulus
+    // converter warps writing each of K and V: 128-position chunks give every
+    // converter thread one K row and one V row; 64-position chunks give warps
+    // 6-7 the K rows and warps 8-9 the V rows
+    static constexpr int kConvWarpsK = kNc == 128 ? 4 : 2;
+    // 128-position chunks release the K and V halves of a 16-bit stage
+    // separately (K after S, V after PV); 64-position chunks release the stage
+    // as one after PV (measured faster there)
+    static constexpr bool kKVSplit = kNc == 128;
+    static constexpr int kKBytes = kNc * D * 2;         // one K (or V) chunk
     static constexpr int kStageBytes = 2 * kKBytes;
-    static constexpr int kF8Bytes = 2 * kN * D;         // one 8-bit K + V chunk
+    static constexpr int kF8Bytes = 2 * kNc * D;        // one 8-bit K + V chunk
     static constexpr int kStageOff = 0;
     static constexpr int kF8Off = kStageOff + kStages * kStageBytes;
     static constexpr int kBarOff = kF8Off + kF8Stages * kF8Bytes;
     static constexpr int kSmemBytes = kBarOff + 512 + 1024;   // + barriers + alignment slack
     // Tensor memory (32-bit columns x 128 lanes; lane = query row of the tile):
-    // S double buffer, O accumulator, Q and a double-buffered P as 16-bit pairs
-    // (the A operands of the two MMAs).
+    // S double buffer, O accumulator, Q and P as 16-bit pairs (the A operands of
+    // the two MMAs).  64-position chunks: P has its own double buffer;
+    // 128-position chunks: P is written over the first half of its chunk's S
+    // buffer (the four would not fit in 512 columns).
+    static constexpr bool kAliasP = kNc == 128;
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t kSCol = 0;                // 2 x kN
-    static constexpr uint32_t kOCol = 2 * kN;           // D (<= 128)
+    static constexpr uint32_t kSCol = 0;                // 2 x kNc
+    static constexpr uint32_t kOCol = 2 * kNc;          // D (<= 128)
     static constexpr uint32_t kQCol = kOCol + 128;      // D / 2
-    static constexpr uint32_t kPCol = kQCol + 64;       // 2 x kN / 2
+    static constexpr uint32_t kPCol = kAliasP ? kSCol : kQCol + 64;
+    static constexpr uint32_t kPStride = kAliasP ? kNc : kNc / 2;   // columns between P buffers
 };
 
 struct TcArgs {
@@ -108,8 +127,10 @@ struct TcArgs {
 };
 
 struct Barriers {
-    uint64_t kv_full[8];
+    uint64_t kv_full[8];      // FP8: the K half of the stage
     uint64_t kv_empty[8];
+    uint64_t v_full[8];       // FP8 only: the V half of the stage
+    uint64_t v_empty[8];
     uint64_t s_full[2];
     uint64_t s_free[2];
     uint64_t p_full[2];
@@ -138,6 +159,7 @@ struct UnitGeo {
     int n_splits;
 };
 
+template <int NC>
 __device__ __forceinline__ UnitGeo unit_geo(const TcArgs& a, int u)
 {
     UnitGeo g;
@@ -165,7 +187,7 @@ __device__ __forceinline__ UnitGeo unit_geo(const TcArgs& a, int u)
         const int row0 = g.tile * kM;
         if (row0 < g.n_rows && g.split == 0) {
             const int t_max = (min(g.n_rows, row0 + kM) - 1) / a.G;
-            g.n_ctx = t_max / kN + 1;
+            g.n_ctx = t_max / NC + 1;
             g.live = true;
         }
     } else {
@@ -186,7 +208,7 @@ __device__ __forceinline__ UnitGeo unit_geo(const TcArgs& a, int u)
         if (bad) { g.C = 0; g.Pb = 0; }
         g.n_rows = g.Pb * a.G;
         const int row0 = g.tile * kM;
-        const int n_cc = (g.C + kN - 1) / kN;
+        const int n_cc = (g.C + NC - 1) / NC;
         g.n_splits = max(1, (n_cc + a.chunks_per_split - 1) / a.chunks_per_split);
         if (row0 >= g.n_rows) {
             g.zero_tile = g.split == 0 && row0 < a.P_max * a.G;
@@ -194,7 +216,7 @@ __device__ __forceinline__ UnitGeo unit_geo(const TcArgs& a, int u)
             g.live = true;
             g.c_first = g.split * a.chunks_per_split;
             g.n_ctx = max(0, min(n_cc, g.c_first + a.chunks_per_split) - g.c_first);
-            if (g.split == g.n_splits - 1) g.n_draft = (g.Pb + kN - 1) / kN;
+            if (g.split == g.n_splits - 1) g.n_draft = (g.Pb + NC - 1) / NC;
         }
     }
     if (bad && g.h == 0 && g.tile == 0 && g.split == 0 && threadIdx.x == 0)
@@ -275,8 +297,12 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
 
     if (tid == 0) {
         for (int i = 0; i < C::kStages; ++i) {
-            mbar_init(&bar.kv_full[i], F8 ? 4 : 1);        // F8: the four converter warps
+            // FP8: the converter warps that write K (all four for 128-position
+            // chunks, 6-7 for 64-position chunks) and those that write V
+            mbar_init(&bar.kv_full[i], F8 ? (C::kKVSplit ? C::kConvWarpsK : 4) : 1);
             mbar_init(&bar.kv_empty[i], F8 ? 1 : 2);       // bf16: K read by S, V read by PV
+            mbar_init(&bar.v_full[i], C::kConvWarpsK);
+            mbar_init(&bar.v_empty[i], 1);
         }
         for (int i = 0; i < C::kF8Stages; ++i) {
             mbar_init(&bar.f8_full[i], 1);
@@ -321,90 +347,132 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
         if (lane == 0) {
             uint32_t g8 = 0;                              // context chunks only
             for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
-                const UnitGeo geo = unit_geo(a, u);
+                const UnitGeo geo = unit_geo<C::kNc>(a, u);
                 if (!geo.live) continue;
                 bool ok = true;
                 for (int j = 0; j < geo.n_ctx; ++j, ++g8) {
-                    const int st = g8 % C::kF8Stages;
-                    if (g8 >= (uint32_t)C::kF8Stages &&
-                        !mbar_wait(&bar.f8_empty[st], ((g8 / C::kF8Stages) - 1) & 1, abort, kWaitBudget)) {
+                    const int st = g8 % C::kF8Ring;
+                    if (g8 >= (uint32_t)C::kF8Ring &&
+                        !mbar_wait(&bar.f8_empty[st], ((g8 / C::kF8Ring) - 1) & 1, abort, kWaitBudget)) {
                         ok = false;
                         break;
                     }
                     unsigned char* dst = smem + C::kF8Off + st * C::kF8Bytes;
                     mbar_arrive_expect_tx(&bar.f8_full[st], C::kF8Bytes);
-                    const int z = (int)(geo.kv_base + (int64_t)(geo.c_first + j) * kN);
+                    const int z = (int)(geo.kv_base + (int64_t)(geo.c_first + j) * C::kNc);
                     tma_load_3d(dst, &map_kc, &bar.f8_full[st], 0, geo.h, z);
-                    tma_load_3d(dst + kN * D, &map_vc, &bar.f8_full[st], 0, geo.h, z);
+                    tma_load_3d(dst + C::kNc * D, &map_vc, &bar.f8_full[st], 0, geo.h, z);
                 }
                 if (!ok) { fail(); break; }
             }
-            const uint32_t first = g8 > (uint32_t)C::kF8Stages ? g8 - C::kF8Stages : 0u;
+            const uint32_t first = g8 > (uint32_t)C::kF8Ring ? g8 - C::kF8Ring : 0u;
             for (uint32_t k = first; k < g8; ++k)
-                mbar_wait(&bar.f8_full[k % C::kF8Stages], (k / C::kF8Stages) & 1, &no_abort, kWaitBudget);
+                mbar_wait(&bar.f8_full[k % C::kF8Ring], (k / C::kF8Ring) & 1, &no_abort, kWaitBudget);
         }
     } else if (F8 && warp >= kConvWarp0) {
         // ------------------------------------------------------------ converters
-        // thread ct: row ct % 64 of K (ct < 64) or V of every chunk
+        // K and V halves of a 16-bit stage are filled and released separately: K
+        // as soon as S has read it, V once PV has.  128-position chunks: thread
+        // ct converts row ct of K and of V; 64-position chunks: threads 0-63
+        // convert the K rows, threads 64-127 the V rows.
         const int ct = tid - kConvWarp0 * 32;
-        const int is_v = ct >> 6, row = ct & 63;
+        constexpr bool kHalves = C::kNc == 64;
+        const int row = kHalves ? (ct & 63) : ct;
+        const bool do_k = !kHalves || ct < 64;     // warp-uniform
+        const bool do_v = !kHalves || ct >= 64;
         uint32_t g = 0, g8 = 0;
+        // one 128-byte e4m3 row (swizzled) -> one 256-byte f16 row in two 128-byte blocks
+        auto widen_row = [&](const unsigned char* src, unsigned char* dst) {
+#pragma unroll
+            for (int c = 0; c < D / 16; ++c) {
+                const uint4 x = *reinterpret_cast<const uint4*>(src + sw128(row, c));
+                uint4 lo, hi;
+                lo.x = e4m3x2_to_f16x2(x.x & 0xffffu); lo.y = e4m3x2_to_f16x2(x.x >> 16);
+                lo.z = e4m3x2_to_f16x2(x.y & 0xffffu); lo.w = e4m3x2_to_f16x2(x.y >> 16);
+                hi.x = e4m3x2_to_f16x2(x.z & 0xffffu); hi.y = e4m3x2_to_f16x2(x.z >> 16);
+                hi.z = e4m3x2_to_f16x2(x.w & 0xffffu); hi.w = e4m3x2_to_f16x2(x.w >> 16);
+                const int c16 = 2 * c;              // two 16-bit chunks of 8 values
+                *reinterpret_cast<uint4*>(dst + (c16 >> 3) * (C::kNc * 128) + sw128(row, c16 & 7)) = lo;
+                *reinterpret_cast<uint4*>(dst + ((c16 + 1) >> 3) * (C::kNc * 128) +
+                                          sw128(row, (c16 + 1) & 7)) = hi;
+            }
+        };
+        // one bf16 draft row times a scale -> f16
+        auto draft_row = [&](const uint16_t* base, const UnitGeo& geo, int d, float sc,
+                             unsigned char* dst) {
+            const uint4* src = d < geo.Pb
+                ? reinterpret_cast<const uint4*>(base + (((size_t)geo.b * a.P_max + d) * a.Hkv + geo.h) * D)
+                : nullptr;
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) {
+                uint4 y = make_uint4(0, 0, 0, 0);
+                if (src) {
+                    const uint4 x = __ldg(src + c);
+                    y.x = bf16x2_to_f16x2(x.x, sc); y.y = bf16x2_to_f16x2(x.y, sc);
+                    y.z = bf16x2_to_f16x2(x.z, sc); y.w = bf16x2_to_f16x2(x.w, sc);
+                }
+                *reinterpret_cast<uint4*>(dst + (c >> 3) * (C::kNc * 128) + sw128(row, c & 7)) = y;
+            }
+        };
         for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
-            const UnitGeo geo = unit_geo(a, u);
+            const UnitGeo geo = unit_geo<C::kNc>(a, u);
             if (!geo.live) continue;
             const int n = geo.n_ctx + geo.n_draft;
             bool ok = true;
             for (int j = 0; j < n; ++j, ++g) {
                 const int st = g % C::kStages;
-                if (g >= (uint32_t)C::kStages &&
-                    !warp_wait(&bar.kv_empty[st], ((g / C::kStages) - 1) & 1, abort, kWaitBudget)) {
+                const uint32_t prev = ((g / C::kStages) - 1) & 1;
+                unsigned char* kdst = smem + C::kStageOff + st * C::kStageBytes;
+                unsigned char* vdst = kdst + C::kKBytes;
+                const bool ctx = j < geo.n_ctx;
+                const int s8 = g8 % C::kF8Ring;
+                const unsigned char* src = smem + C::kF8Off + s8 * C::kF8Bytes;
+                if (ctx && !warp_wait(&bar.f8_full[s8], (g8 / C::kF8Ring) & 1, abort, kWaitBudget)) {
                     ok = false;
                     break;
                 }
-                unsigned char* dst = smem + C::kStageOff + st * C::kStageBytes + is_v * C::kKBytes;
-                if (j < geo.n_ctx) {
-                    const int s8 = g8 % C::kF8Stages;
-                    if (!warp_wait(&bar.f8_full[s8], (g8 / C::kF8Stages) & 1, abort, kWaitBudget)) {
+                if (!C::kKVSplit && g >= (uint32_t)C::kStages &&
+                    !warp_wait(&bar.kv_empty[st], prev, abort, kWaitBudget)) {
+                    ok = false;
+                    break;
+                }
+                // ---- K half ----
+                if (do_k) {
+                    if (C::kKVSplit && g >= (uint32_t)C::kStages &&
+                        !warp_wait(&bar.kv_empty[st], prev, abort, kWaitBudget)) {
                         ok = false;
                         break;
                     }
-                    const unsigned char* src = smem + C::kF8Off + s8 * C::kF8Bytes + is_v * (kN * D);
-#pragma unroll
-                    for (int c = 0; c < D / 16; ++c) {      // 16 e4m3 values = 16 B (swizzled row)
-                        const uint4 x = *reinterpret_cast<const uint4*>(src + sw128(row, c));
-                        uint4 lo, hi;
-                        lo.x = e4m3x2_to_f16x2(x.x & 0xffffu); lo.y = e4m3x2_to_f16x2(x.x >> 16);
-                        lo.z = e4m3x2_to_f16x2(x.y & 0xffffu); lo.w = e4m3x2_to_f16x2(x.y >> 16);
-                        hi.x = e4m3x2_to_f16x2(x.z & 0xffffu); hi.y = e4m3x2_to_f16x2(x.z >> 16);
-                        hi.z = e4m3x2_to_f16x2(x.w & 0xffffu); hi.w = e4m3x2_to_f16x2(x.w >> 16);
-                        const int c16 = 2 * c;              // two 16-bit chunks of 8 values
-                        *reinterpret_cast<uint4*>(dst + (c16 >> 3) * (kN * 128) + sw128(row, c16 & 7)) = lo;
-                        *reinterpret_cast<uint4*>(dst + ((c16 + 1) >> 3) * (kN * 128) + sw128(row, (c16 + 1) & 7)) = hi;
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bar.f8_empty[s8]);
-                    ++g8;
-                } else {
-                    const int d = (j - geo.n_ctx) * kN + row;   // draft row
-                    const float sc = is_v ? a.v_inv : a.k_inv;
-                    const uint4* src = d < geo.Pb
-                        ? reinterpret_cast<const uint4*>((is_v ? a.v_new : a.k_new) +
-                                                         (((size_t)geo.b * a.P_max + d) * a.Hkv + geo.h) * D)
-                        : nullptr;
-#pragma unroll
-                    for (int c = 0; c < D / 8; ++c) {
-                        uint4 y = make_uint4(0, 0, 0, 0);
-                        if (src) {
-                            const uint4 x = __ldg(src + c);
-                            y.x = bf16x2_to_f16x2(x.x, sc); y.y = bf16x2_to_f16x2(x.y, sc);
-                            y.z = bf16x2_to_f16x2(x.z, sc); y.w = bf16x2_to_f16x2(x.w, sc);
-                        }
-                        *reinterpret_cast<uint4*>(dst + (c >> 3) * (kN * 128) + sw128(row, c & 7)) = y;
+                    if (ctx) widen_row(src, kdst);
+                    else draft_row(a.k_new, geo, (j - geo.n_ctx) * C::kNc + row, a.k_inv, kdst);
+                    if (C::kKVSplit) {
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bar.kv_full[st]);
                     }
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar.kv_full[st]);
+                // ---- V half ----
+                if (do_v) {
+                    if (C::kKVSplit && g >= (uint32_t)C::kStages &&
+                        !warp_wait(&bar.v_empty[st], prev, abort, kWaitBudget)) {
+                        ok = false;
+                        break;
+                    }
+                    if (ctx) widen_row(src + C::kNc * D, vdst);
+                    else draft_row(a.v_new, geo, (j - geo.n_ctx) * C::kNc + row, a.v_inv, vdst);
+                    if (C::kKVSplit) {
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bar.v_full[st]);
+                    }
+                }
+                if (!C::kKVSplit) {                 // the whole stage at once
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar.kv_full[st]);
+                }
+                if (ctx && lane == 0) mbar_arrive(&bar.f8_empty[s8]);
+                if (ctx) ++g8;
             }
             if (!ok) { fail(); break; }
         }
@@ -413,7 +481,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
         if (lane == 0) {
             uint32_t g = 0;                               // global chunk counter
             for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
-                const UnitGeo geo = unit_geo(a, u);
+                const UnitGeo geo = unit_geo<C::kNc>(a, u);
                 if (!geo.live) continue;
                 const int n = geo.n_ctx + geo.n_draft;
                 // first cache row of context chunk j (paged: looked up one chunk ahead,
@@ -466,39 +534,40 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
         // bf16: S = Q K^T only (the PV issuer runs in its own warp, so the two
         // chains overlap); FP8: S and O += P V from this one thread.
         if (lane == 0) {
-            constexpr uint32_t idS = F8 ? idesc_f16(kM, kN, false, false) : idesc_bf16(kM, kN, false, false);
+            constexpr uint32_t idS = F8 ? idesc_f16(kM, C::kNc, false, false) : idesc_bf16(kM, C::kNc, false, false);
             constexpr uint32_t idPV = F8 ? idesc_f16(kM, D, false, true) : idesc_bf16(kM, D, false, true);
             uint32_t g = 0, unit_iter = 0;
             // Shared-memory descriptors differ only in their start-address field
             // (bits 0-13, address >> 4): build each base once and add offsets,
             // which keeps the issuing thread's work per MMA to two additions.
             const uint64_t k_desc = smem_desc(smem_addr(smem + C::kStageOff), 16, 1024, kSwizzle128B);
-            const uint64_t v_desc = smem_desc(smem_addr(smem + C::kStageOff + C::kKBytes), kN * 128,
+            const uint64_t v_desc = smem_desc(smem_addr(smem + C::kStageOff + C::kKBytes), C::kNc * 128,
                                               1024, kSwizzle128B);
             // S = Q K^T for chunk gs (D/16 K-steps) into TMEM tile gs & 1.
             auto issue_s = [&](uint32_t gs) {
                 const uint64_t kd = k_desc + (uint64_t)(((gs % C::kStages) * C::kStageBytes) >> 4);
-                const uint32_t d_tmem = tmem + C::kSCol + (gs & 1) * kN;
+                const uint32_t d_tmem = tmem + C::kSCol + (gs & 1) * C::kNc;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = ((ks >> 2) * (kN * 128) + (ks & 3) * 32) >> 4;
+                    const uint32_t off = ((ks >> 2) * (C::kNc * 128) + (ks & 3) * 32) >> 4;
                     mma_tmem_a(d_tmem, tmem + C::kQCol + ks * 8, kd + off, idS, ks > 0);
                 }
                 mma_commit(&bar.s_full[gs & 1]);
             };
-            // O += P V for chunk gp (4 K-steps of 16 positions).
+            // O += P V for chunk gp (K-steps of 16 positions).
             auto issue_pv = [&](uint32_t gp, bool first) {
                 const uint64_t vd = v_desc + (uint64_t)(((gp % C::kStages) * C::kStageBytes) >> 4);
-                const uint32_t pt = tmem + C::kPCol + (gp & 1) * (kN / 2);
+                const uint32_t pt = tmem + C::kPCol + (gp & 1) * C::kPStride;
 #pragma unroll
-                for (int kk = 0; kk < kN / 16; ++kk)
+                for (int kk = 0; kk < C::kNc / 16; ++kk)
                     mma_tmem_a(tmem + C::kOCol, pt + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), idPV,
                                !(first && kk == 0));
-                mma_commit(&bar.kv_empty[gp % C::kStages]);
+                mma_commit(C::kKVSplit ? &bar.v_empty[gp % C::kStages] : &bar.kv_empty[gp % C::kStages]);
+                mma_commit(&bar.p_free[gp & 1]);
                 mma_commit(&bar.pv_done);
             };
             for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
-                const UnitGeo geo = unit_geo(a, u);
+                const UnitGeo geo = unit_geo<C::kNc>(a, u);
                 if (!geo.live) continue;
                 const int n = geo.n_ctx + geo.n_draft;
                 if (!mbar_wait(&bar.q_full, unit_iter & 1, abort, kWaitBudget)) { fail(); break; }
@@ -508,17 +577,24 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 // then PV_{j-1} once the softmax has written P_{j-1}.
                 for (int j = 0; j < n && ok; ++j) {
                     const uint32_t gg = g + j;
+                    // 128-position chunks: P_{j-2} lives in the S buffer that S_j
+                    // overwrites, so S_j also waits for PV_{j-2} to complete
                     if (!mbar_wait(&bar.kv_full[gg % C::kStages], (gg / C::kStages) & 1, abort, kWaitBudget) ||
-                        (gg >= 2 && !mbar_wait(&bar.s_free[gg & 1], ((gg >> 1) - 1) & 1, abort, kWaitBudget))) {
+                        (gg >= 2 && !mbar_wait(&bar.s_free[gg & 1], ((gg >> 1) - 1) & 1, abort, kWaitBudget)) ||
+                        (C::kAliasP && gg >= 2 &&
+                         !mbar_wait(&bar.p_free[gg & 1], ((gg >> 1) - 1) & 1, abort, kWaitBudget))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     issue_s(gg);
-                    if constexpr (!F8) {
+                    if (!F8 || C::kKVSplit)
                         mma_commit(&bar.kv_empty[gg % C::kStages]);     // K of the stage read
-                    } else if (j >= 1) {
-                        if (!mbar_wait(&bar.p_full[(gg - 1) & 1], ((gg - 1) >> 1) & 1, abort, kWaitBudget)) {
+                    if (F8 && j >= 1) {
+                        const uint32_t gp = gg - 1;
+                        if (!mbar_wait(&bar.p_full[gp & 1], (gp >> 1) & 1, abort, kWaitBudget) ||
+                            (C::kKVSplit && !mbar_wait(&bar.v_full[gp % C::kStages], (gp / C::kStages) & 1,
+                                                       abort, kWaitBudget))) {
                             ok = false;
                             break;
                         }
@@ -529,7 +605,10 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 if constexpr (F8) {
                     if (ok) {
                         const uint32_t gl = g + n - 1;
-                        if (!mbar_wait(&bar.p_full[gl & 1], (gl >> 1) & 1, abort, kWaitBudget)) ok = false;
+                        if (!mbar_wait(&bar.p_full[gl & 1], (gl >> 1) & 1, abort, kWaitBudget) ||
+                            (C::kKVSplit && !mbar_wait(&bar.v_full[gl % C::kStages], (gl / C::kStages) & 1,
+                                                       abort, kWaitBudget)))
+                            ok = false;
                         else {
                             tc_fence_after();
                             issue_pv(gl, n == 1);
@@ -553,10 +632,10 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
         if (lane == 0) {
             constexpr uint32_t idPV = idesc_bf16(kM, D, false, true);
             uint32_t g = 0;
-            const uint64_t v_desc = smem_desc(smem_addr(smem + C::kStageOff + C::kKBytes), kN * 128,
+            const uint64_t v_desc = smem_desc(smem_addr(smem + C::kStageOff + C::kKBytes), C::kNc * 128,
                                               1024, kSwizzle128B);
             for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
-                const UnitGeo geo = unit_geo(a, u);
+                const UnitGeo geo = unit_geo<C::kNc>(a, u);
                 if (!geo.live) continue;
                 const int n = geo.n_ctx + geo.n_draft;
                 bool ok = true;
@@ -568,9 +647,9 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                     }
                     tc_fence_after();
                     const uint64_t vd = v_desc + (uint64_t)(((gg % C::kStages) * C::kStageBytes) >> 4);
-                    const uint32_t pt = tmem + C::kPCol + (gg & 1) * (kN / 2);
+                    const uint32_t pt = tmem + C::kPCol + (gg & 1) * C::kPStride;
 #pragma unroll
-                    for (int kk = 0; kk < kN / 16; ++kk)
+                    for (int kk = 0; kk < C::kNc / 16; ++kk)
                         mma_tmem_a(tmem + C::kOCol, pt + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), idPV,
                                    !(j == 0 && kk == 0));
                     mma_commit(&bar.kv_empty[gg % C::kStages]);
@@ -589,7 +668,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         uint32_t g = 0, unit_iter = 0;
         for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
-            const UnitGeo geo = unit_geo(a, u);
+            const UnitGeo geo = unit_geo<C::kNc>(a, u);
             const int row = geo.tile * kM + t;
             const int hq0 = geo.h * a.G;
             if (geo.zero_tile) {                           // padded rows of a tree tile
@@ -646,6 +725,8 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 const int sb = gg & 1;
                 if (!warp_wait(&bar.s_full[sb], (gg >> 1) & 1, abort, kWaitBudget)) { ok = false; break; }
                 tc_fence_after();
+                constexpr int kH = C::kNc / 64;            // 64-column parts of a chunk
+                const uint32_t p_col = tmem + lane_base + C::kPCol + sb * C::kPStride;
                 if (dead) {
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bar.s_free[sb]);
@@ -658,11 +739,14 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                         break;
                     }
                     tc_fence_after();
-                    if (j < 2) {
+                    // zero P rows once per buffer and unit, or every chunk when P
+                    // shares its columns with S, which the MMA rewrites
+                    if (C::kAliasP || j < 2) {
                         uint32_t zero[32];
 #pragma unroll
                         for (int c = 0; c < 32; ++c) zero[c] = 0u;
-                        tmem_st32(tmem + lane_base + C::kPCol + sb * (kN / 2), zero);
+#pragma unroll
+                        for (int h = 0; h < kH; ++h) tmem_st32(p_col + h * 32, zero);
                         tmem_st_wait();
                     }
                     tc_fence_before();
@@ -670,47 +754,61 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                     if (lane == 0) mbar_arrive(&bar.p_full[sb]);
                     continue;
                 }
-                uint32_t sr[64];
-                tmem_ld32(tmem + lane_base + C::kSCol + sb * kN, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-                tmem_ld32(tmem + lane_base + C::kSCol + sb * kN + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-                tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar.s_free[sb]);
+                // scores of part h (64 columns) from TMEM
+                auto load_part = [&](int h, float (&s)[64]) {
+                    uint32_t sr[64];
+                    const uint32_t s_col = tmem + lane_base + C::kSCol + sb * C::kNc + h * 64;
+                    tmem_ld32(s_col, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+                    tmem_ld32(s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c]);
+                };
+                // ---- visibility of part h -------------------------------------------
+                auto mask_part = [&](int h, float (&s)[64]) {
+                    if (!valid) {
+#pragma unroll
+                        for (int c = 0; c < 64; ++c) s[c] = -INFINITY;
+                    } else if (j < geo.n_ctx) {
+                        const int pos0 = (geo.c_first + j) * C::kNc + h * 64;
+                        const int lim = a.causal ? min(geo.C, qpos + 1) : geo.C;   // visible: pos < lim
+                        if (pos0 + 64 > lim) {
+#pragma unroll
+                            for (int c = 0; c < 64; ++c)
+                                if (pos0 + c >= lim) s[c] = -INFINITY;
+                        }
+                    } else {
+                        const int d0 = (j - geo.n_ctx) * C::kNc + h * 64;
+                        const uint32_t w0 = (d0 >> 5) < a.mask_words ? __ldg(mrow + (d0 >> 5)) : 0u;
+                        const uint32_t w1 = (d0 >> 5) + 1 < a.mask_words ? __ldg(mrow + (d0 >> 5) + 1) : 0u;
+#pragma unroll
+                        for (int c = 0; c < 64; ++c) {
+                            const uint32_t w = c < 32 ? w0 : w1;
+                            const bool vis = (d0 + c < geo.Pb) && ((w >> (c & 31)) & 1u);
+                            if (!vis) s[c] = -INFINITY;
+                        }
+                    }
+                };
                 float s[64];
+                float mx = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c]);
-                // ---- visibility -----------------------------------------------
-                if (!valid) {
-#pragma unroll
-                    for (int c = 0; c < 64; ++c) s[c] = -INFINITY;
-                } else if (j < geo.n_ctx) {
-                    const int pos0 = (geo.c_first + j) * kN;
-                    const int lim = a.causal ? min(geo.C, qpos + 1) : geo.C;   // visible: pos < lim
-                    if (pos0 + kN > lim) {
-#pragma unroll
-                        for (int c = 0; c < 64; ++c)
-                            if (pos0 + c >= lim) s[c] = -INFINITY;
+                for (int h = 0; h < kH; ++h) {
+                    load_part(h, s);
+                    if (kH == 1) {                         // S is in registers: release it
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bar.s_free[sb]);
                     }
-                } else {
-                    const int d0 = (j - geo.n_ctx) * kN;
-                    const uint32_t w0 = (d0 >> 5) < a.mask_words ? __ldg(mrow + (d0 >> 5)) : 0u;
-                    const uint32_t w1 = (d0 >> 5) + 1 < a.mask_words ? __ldg(mrow + (d0 >> 5) + 1) : 0u;
+                    mask_part(h, s);
+                    // ---- online softmax (log2 domain) ----------------------------
+                    float mx8[8];
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) {
-                        const uint32_t w = c < 32 ? w0 : w1;
-                        const bool vis = (d0 + c < geo.Pb) && ((w >> (c & 31)) & 1u);
-                        if (!vis) s[c] = -INFINITY;
-                    }
+                    for (int e = 0; e < 8; ++e) mx8[e] = s[e];
+#pragma unroll
+                    for (int c = 8; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+                    mx = fmaxf(mx, fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                         fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))));
                 }
-                // ---- online softmax (log2 domain) ------------------------------
-                float mx8[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) mx8[e] = s[e];
-#pragma unroll
-                for (int c = 8; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
-                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
                 const float ms = mx * a.scale_log2;
                 const bool need = ms > m + kRescaleThreshold;
                 const float m_new = need ? ms : m;
@@ -741,33 +839,46 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 }
                 const float base = (m == -INFINITY) ? 0.f : m;
                 float lsum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                uint32_t pv[32];
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
-                    float p[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        p[e] = fast_exp2(fmaf(s[c8 * 8 + e], a.scale_log2, -base));
-                        lsum[e] += p[e];
+                for (int h = 0; h < kH; ++h) {
+                    if (kH > 1) {                          // FP8: read part h again
+                        load_part(h, s);
+                        mask_part(h, s);
                     }
+                    uint32_t pv[32];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) pv[c8 * 4 + e] = pack16<F8>(p[2 * e], p[2 * e + 1]);
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        float p[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            p[e] = fast_exp2(fmaf(s[c8 * 8 + e], a.scale_log2, -base));
+                            lsum[e] += p[e];
+                        }
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) pv[c8 * 4 + e] = pack16<F8>(p[2 * e], p[2 * e + 1]);
+                    }
+                    // P (16-bit) into this lane's P columns: PV's A operand (bf16: once
+                    // PV of the chunk two back has released that buffer; FP8: S_j was
+                    // issued after PV_{j-2}, and s_full(j) covers the completion of every
+                    // earlier MMA of that issuer; with P over S, part h overwrites only
+                    // S columns already read)
+                    if (h == 0) {
+                        if (!F8 && gg >= 2 &&
+                            !warp_wait(&bar.p_free[sb], ((gg >> 1) - 1) & 1, abort, kWaitBudget)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+                    tmem_st32(p_col + h * 32, pv);
                 }
-                // P (16-bit) into this lane's half of the P buffer: PV's A operand
-                // (bf16: once PV of the chunk two back has released that buffer;
-                // FP8: S_j was issued after PV_{j-2}, so that is already true)
-                if (!F8 && gg >= 2 &&
-                    !warp_wait(&bar.p_free[sb], ((gg >> 1) - 1) & 1, abort, kWaitBudget)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                tmem_st32(tmem + lane_base + C::kPCol + sb * (kN / 2), pv);
+                if (!ok) break;
                 l += ((lsum[0] + lsum[1]) + (lsum[2] + lsum[3])) +
                      ((lsum[4] + lsum[5]) + (lsum[6] + lsum[7]));
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
+                if (kH > 1 && lane == 0) mbar_arrive(&bar.s_free[sb]);
                 if (lane == 0) mbar_arrive(&bar.p_full[sb]);
             }
             if (!ok || !warp_wait(&bar.o_final, unit_iter & 1, abort, kWaitBudget)) { fail(); break; }
@@ -910,14 +1021,14 @@ bool make_kv_map(CUtensorMap* map, const void* base, int64_t rows, int heads, in
     return r == CUDA_SUCCESS;
 }
 
-// [rows, heads, D] e4m3 -> boxes of 64 positions x 1 head x D bytes, 128-byte swizzle
+// [rows, heads, D] e4m3 -> boxes of 128 positions x 1 head x D bytes, 128-byte swizzle
 bool make_fp8_map(CUtensorMap* map, const void* base, int64_t rows, int heads, int D)
 {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
     cuuint64_t strides[2] = {(cuuint64_t)D, (cuuint64_t)heads * D};
-    cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)kN};
+    cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)Cfg<128, true>::kNc};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1019,6 +1130,17 @@ cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, in
         a.v_inv = 1.f / fp8->v_scale;
         a.out_scale = fp8->v_scale;
         a.scale_log2 *= fp8->k_scale;
+    }
+    if (fp8 != nullptr) {
+        // 128-position chunks: the same split lengths rounded up to whole chunks,
+        // so the splits (and the partials) never exceed the plan's; the workspace
+        // keeps the plan's layout below
+        constexpr int nc = Cfg<128, true>::kNc;
+        const long cc = ((long)max_kv + nc - 1) / nc;
+        const long cps = std::max<long>(1, ((long)plan.split_len + nc - 1) / nc);
+        a.chunks_per_split = (int)cps;
+        a.splits = (int)std::max<long>(1, (cc + cps - 1) / cps);
+        a.n_units = B * Hkv * plan.tiles * a.splits;
     }
     if (plan.splits > 1) {
         const size_t unit_rows = (size_t)B * Hkv * plan.tiles * kM;
