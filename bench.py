@@ -55,6 +55,8 @@ def _args():
     ap.add_argument("--cpu-sample-requests", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-next-rows", action="store_true",
+                    help="skip timing the calls beyond the verification step")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's request count (small profiling runs)")
     return ap.parse_args()
@@ -253,6 +255,89 @@ def run_reference(args):
 # ----------------------------------------------------------------------------
 # our CUDA path
 # ----------------------------------------------------------------------------
+def _time_us(fn, n: int = 20) -> float:
+    """Mean device time of one call, n calls back to back on the current stream
+    (CUDA events, after three warm-up calls)."""
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n * 1e3
+
+
+def measure_next_rows(cfg, inp, step, dev, peak: float) -> dict:
+    """The calls beyond the verification step, timed on the same workload's
+    tensors after the timed region: FP8 and paged-cache attention, stochastic
+    verification, commit of the accepted path, and one drafter beam-search step."""
+    import tree_attention_verify_gb300 as rd
+    rows = {}
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    pk, acc = step.pk, step.acc
+    max_ctx = max(1, int(inp["ctx_lens"].max()))
+    ws = torch.zeros(max(16, rd.rd_tree_attention_workspace_size(
+        cfg.B, cfg.P_max, cfg.Hq, cfg.Hkv, cfg.D, max_ctx)), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(inp["q"])
+    plen = pk["packed_len"].cpu().numpy()
+    bf16_bytes = attention_bytes(cfg, inp["ctx_lens"], plen)
+    ctx_kv = cfg.Hkv * 4.0 * cfg.D * float(np.asarray(inp["ctx_lens"], np.float64).sum())
+    # FP8 (e4m3) context cache: context K/V bytes halve
+    kc, ks = workloads.make_fp8_cache(inp["k_cache"])
+    vc, vs = workloads.make_fp8_cache(inp["v_cache"])
+    us = _time_us(lambda: rd.rd_tree_attention_fp8(
+        inp["q"], inp["k_draft"], inp["v_draft"], kc, vc, ks, vs, inp["ctx_offsets"],
+        pk["packed_len"], pk["mask"], max_ctx=max_ctx, out=o, workspace=ws, dev_status=st))
+    b8 = bf16_bytes - ctx_kv / 2
+    rows["rd_tree_attention_fp8"] = {"us": us, "gbs": b8 / us / 1e3, "frac": b8 / us / 1e3 / peak,
+                                     "algorithmic_bytes": b8}
+    del kc, vc
+    # paged cache (256-position pages in a shuffled pool)
+    pg = workloads.make_paged(inp["k_cache"], inp["v_cache"], inp["ctx_lens"], 256,
+                              np.random.default_rng(cfg.seed + 5))
+    us = _time_us(lambda: rd.rd_tree_attention_paged(
+        inp["q"], inp["k_draft"], inp["v_draft"], pg["k_pool"], pg["v_pool"], pg["block_table"],
+        pg["ctx_lens"], pk["packed_len"], pk["mask"], max_ctx=max_ctx, out=o, workspace=ws,
+        dev_status=st))
+    rows["rd_tree_attention_paged"] = {"us": us, "gbs": bf16_bytes / us / 1e3,
+                                       "frac": bf16_bytes / us / 1e3 / peak, "page_size": 256}
+    # commit of the accepted path into the paged cache (idempotent: lengths not advanced)
+    new_lens = torch.empty_like(pg["ctx_lens"])
+    us = _time_us(lambda: rd.rd_commit_accepted(
+        inp["k_draft"], inp["v_draft"], pk["unpacker"], acc["best_beam"], acc["n_accepted"],
+        pg["k_pool"], pg["v_pool"], pg["block_table"], pg["ctx_lens"], new_ctx_lens=new_lens,
+        dev_status=st))
+    rows["rd_commit_accepted"] = {"us": us}
+    del pg
+    # stochastic verification with drafter logits correlated with the target's
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(cfg.seed + 6)
+    draft = workloads.make_draft_logits(inp["logits"], gen)
+    ua, usm = workloads.make_uniforms(cfg.B, cfg.P_max, cfg.vocab, np.random.default_rng(cfg.seed + 6))
+    ua, usm = ua.to(dev), usm.to(dev)
+    sout = rd.rd_sample_accept(inp["logits"], draft, 1.0, inp["beams"], pk["packer"],
+                               pk["unpacker"], pk["packed_len"], ua, usm, dev_status=st)
+    us = _time_us(lambda: rd.rd_sample_accept(
+        inp["logits"], draft, 1.0, inp["beams"], pk["packer"], pk["unpacker"], pk["packed_len"],
+        ua, usm, out=sout, dev_status=st))
+    rows["rd_sample_accept"] = {"us": us, "temperature": 1.0,
+                                "mean_accepted": float(sout["n_accepted"].float().mean())}
+    # one drafter beam-search step (W x V candidates per request)
+    lg = (torch.randn((cfg.B, cfg.W, cfg.vocab), generator=gen, device=dev) * 2).to(torch.bfloat16)
+    sc = torch.zeros((cfg.B, cfg.W), dtype=torch.float32, device=dev)
+    bi = inp["beams"][:, :, :cfg.L - 1].contiguous()
+    bout = rd.rd_beam_search_step(lg, sc, bi, dev_status=st)
+    us = _time_us(lambda: rd.rd_beam_search_step(lg, sc, bi, out=bout, dev_status=st))
+    rows["rd_beam_search_step"] = {"us": us, "gbs": lg.numel() * 2 / us / 1e3}
+    torch.cuda.synchronize()
+    if int(st.item()) != 0:
+        raise SystemExit(f"device status {int(st.item())} in the next-row calls")
+    return rows
+
+
 def run_ours(args):
     import tree_attention_verify_gb300 as rd
     from tree_attention_verify_gb300.step import VerifyStep
@@ -321,6 +406,10 @@ def run_ours(args):
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
                 "traffic": _profile_traffic(cfg.name),
                 "algorithmic_bytes_per_launch": attn_bytes}
+
+    next_rows = None
+    if rank == 0 and not args.no_next_rows:
+        next_rows = measure_next_rows(cfg, inp, step, dev, peak)
 
     # ---- end to end through the public API, host buffers ----------------------
     # Every step copies its inputs from pinned host memory and reads its accepted
@@ -408,6 +497,7 @@ def run_ours(args):
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "next_rows": next_rows,
             "gpu_launches": 4 * K,
             "clocks": clk,
         }
