@@ -8,31 +8,42 @@
 // candidates (best first; equal scores go to the lower w*V + v) become the new
 // beams.  A beam whose score is -inf (not live yet) contributes no candidate.
 //
-// One CTA per request.  Pass 1: log-sum-exp of every beam row (fp32).  Pass 2:
-// every thread keeps its best W candidates in registers (insertion), then W
-// rounds of a CTA-wide (max score, min index) reduction pick the winners in
-// order.  No CTA waits for another.
+// One thread-block cluster per request, one CTA per beam row (two rows per CTA
+// when W > 8).  Each CTA streams its row once with 16-byte loads, keeping the
+// running (max, sum of exponentials) and every thread's best W logits (higher
+// value first, lower token on ties); a CTA-wide selection then gives the row's
+// W best tokens, which are also its best candidates since the row's score
+// offset scores_in[w] - lse[w] is common to them.  Rank 0 of the cluster reads
+// every row's log-sum-exp and W candidates from distributed shared memory and
+// picks the request's W best.  No CTA waits for another outside its cluster.
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
 #include "rd_internal.cuh"
 
+namespace cg = cooperative_groups;
+
 namespace {
 
 constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
 constexpr int kNoIndex = 0x7fffffff;
+constexpr int kMaxCluster = 8;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-__device__ __forceinline__ float bf16_at(const uint16_t* row, int v)
-{
-    return __uint_as_float((uint32_t)row[v] << 16);
-}
-
-// candidate order: higher score first, then lower flat index
+// candidate order: higher score first, then lower index
 __device__ __forceinline__ bool before(float s1, int i1, float s2, int i2)
 {
     return s1 > s2 || (s1 == s2 && i1 < i2);
 }
+
+template <int W>
+struct RowOut {
+    float lse;           // natural-log log-sum-exp of the row (-inf: row not live)
+    float val[W];        // the row's W best logits, best first
+    int tok[W];
+};
 
 template <int W>
 __global__ void __launch_bounds__(kThreads)
@@ -41,108 +52,164 @@ beam_step_kernel(const uint16_t* __restrict__ logits, const float* __restrict__ 
                  int32_t* __restrict__ beams_out, float* __restrict__ scores_out,
                  int32_t* __restrict__ parent, int32_t* dev_status)
 {
-    __shared__ float s_red[kThreads / 32];
-    __shared__ float s_bias[W];       // scores_in[w] - lse[w]
+    constexpr int kRowsPerCta = (W + kMaxCluster - 1) / kMaxCluster;
+    __shared__ RowOut<W> s_row[kRowsPerCta];
+    __shared__ float2 s_red[kWarps];
+    __shared__ float s_rs[kWarps];
+    __shared__ int s_ri[kWarps];
     __shared__ float s_win[W];
     __shared__ int s_wi[W];
-    __shared__ float s_rs[kThreads / 32];
-    __shared__ int s_ri[kThreads / 32];
-    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const uint16_t* lg = logits + (size_t)b * W * V;
 
-    // ---- pass 1: log-sum-exp per beam row --------------------------------------
-    for (int w = 0; w < W; ++w) {
-        const uint16_t* row = lg + (size_t)w * V;
-        float mx = -INFINITY;
-        for (int v = tid; v < V; v += kThreads) mx = fmaxf(mx, bf16_at(row, v));
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        if (lane == 0) s_red[warp] = mx;
-        __syncthreads();
-        mx = s_red[0];
-        for (int k = 1; k < kThreads / 32; ++k) mx = fmaxf(mx, s_red[k]);
-        __syncthreads();
-        const float base = mx * kLog2e;
-        float sum = 0.f;
-        for (int v = tid; v < V; v += kThreads) sum += exp2f(fmaf(bf16_at(row, v), kLog2e, -base));
-        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        if (lane == 0) s_red[warp] = sum;
-        __syncthreads();
-        if (tid == 0) {
-            float tot = 0.f;
-            for (int k = 0; k < kThreads / 32; ++k) tot += s_red[k];
-            const float lse = mx + log2f(tot) * kLn2;
-            const float si = scores_in[(size_t)b * W + w];
-            s_bias[w] = (si == -INFINITY) ? -INFINITY : si - lse;
+    const cg::cluster_group cl = cg::this_cluster();
+    const int C = (int)cl.num_blocks();
+    const int rank = (int)cl.block_rank();
+    const int b = blockIdx.x / C;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    // W rounds of a CTA-wide (best score, lowest index) selection over the
+    // threads' sorted lists ls/li; the winners land in s_win / s_wi
+    auto select = [&](float (&ls)[W], int (&li)[W]) {
+        int head = 0;
+        for (int r = 0; r < W; ++r) {
+            float bs = -INFINITY;
+            int bi = kNoIndex;
+#pragma unroll
+            for (int k = 0; k < W; ++k)
+                if (k == head) { bs = ls[k]; bi = li[k]; }
+            float ws = bs;
+            int wi = bi;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float os = __shfl_xor_sync(0xffffffffu, ws, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, wi, o);
+                if (before(os, oi, ws, wi)) { ws = os; wi = oi; }
+            }
+            if (lane == 0) { s_rs[warp] = ws; s_ri[warp] = wi; }
+            __syncthreads();
+            if (tid == 0) {
+                float fs = s_rs[0];
+                int fi = s_ri[0];
+                for (int k = 1; k < kWarps; ++k)
+                    if (before(s_rs[k], s_ri[k], fs, fi)) { fs = s_rs[k]; fi = s_ri[k]; }
+                s_win[r] = fs;
+                s_wi[r] = fi;
+            }
+            __syncthreads();
+            if (bi != kNoIndex && bi == s_wi[r]) ++head;   // the owner of the winner advances
         }
         __syncthreads();
-    }
+    };
 
-    // ---- pass 2: per-thread best W, then W CTA-wide selection rounds ------------
-    float ls[W];
-    int li[W];
+    // ---- this CTA's rows: one pass each --------------------------------------
+    for (int k = 0; k < kRowsPerCta; ++k) {
+        const int w = rank + k * C;
+        RowOut<W>& out = s_row[k];
+        const bool live = w < W && scores_in[(size_t)b * W + w] != -INFINITY;
+        if (!live) {
+            if (tid == 0) out.lse = -INFINITY;
+            continue;
+        }
+        const uint16_t* row = logits + ((size_t)b * W + w) * V;
+        float m = -INFINITY, sum = 0.f;          // log2 units
+        float ls[W];
+        int li[W];
 #pragma unroll
-    for (int k = 0; k < W; ++k) { ls[k] = -INFINITY; li[k] = kNoIndex; }
-    for (int w = 0; w < W; ++w) {
-        const float bias = s_bias[w];
-        if (bias == -INFINITY) continue;
-        const uint16_t* row = lg + (size_t)w * V;
-        for (int v = tid; v < V; v += kThreads) {
-            float cs = bias + bf16_at(row, v);
-            int ci = w * V + v;
-            if (!before(cs, ci, ls[W - 1], li[W - 1])) continue;
+        for (int q = 0; q < W; ++q) { ls[q] = -INFINITY; li[q] = kNoIndex; }
+        auto take = [&](float x, int v) {
+            const float y = x * kLog2e;
+            if (y > m) { sum = (m == -INFINITY) ? 0.f : sum * exp2f(m - y); m = y; }
+            if (y != -INFINITY) sum += exp2f(y - m);
+            if (!before(x, v, ls[W - 1], li[W - 1])) return;
+            float cs = x;
+            int ci = v;
 #pragma unroll
-            for (int k = 0; k < W; ++k) {        // insert into the sorted list
-                if (before(cs, ci, ls[k], li[k])) {
-                    const float ts = ls[k];
-                    const int ti = li[k];
-                    ls[k] = cs; li[k] = ci;
+            for (int q = 0; q < W; ++q) {        // insert into the sorted list
+                if (before(cs, ci, ls[q], li[q])) {
+                    const float ts = ls[q];
+                    const int ti = li[q];
+                    ls[q] = cs; li[q] = ci;
                     cs = ts; ci = ti;
                 }
             }
-        }
-    }
-    int head = 0;
-    for (int r = 0; r < W; ++r) {
-        float bs = -INFINITY;
-        int bi = kNoIndex;
+        };
+        const bool vec = (V % 8 == 0) && (reinterpret_cast<uintptr_t>(row) % 16 == 0);
+        if (vec) {
+            const uint4* r4 = reinterpret_cast<const uint4*>(row);
+            for (int i = tid; i < V / 8; i += kThreads) {
+                const uint4 x = __ldg(r4 + i);
+                const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-        for (int k = 0; k < W; ++k)
-            if (k == head) { bs = ls[k]; bi = li[k]; }
-        float ws = bs;
-        int wi = bi;
-        for (int o = 16; o > 0; o >>= 1) {
-            const float os = __shfl_xor_sync(0xffffffffu, ws, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, wi, o);
-            if (before(os, oi, ws, wi)) { ws = os; wi = oi; }
+                for (int e = 0; e < 4; ++e) {
+                    take(__uint_as_float(xw[e] << 16), i * 8 + 2 * e);
+                    take(__uint_as_float(xw[e] & 0xffff0000u), i * 8 + 2 * e + 1);
+                }
+            }
+        } else {
+            for (int v = tid; v < V; v += kThreads)
+                take(__uint_as_float((uint32_t)__ldg(row + v) << 16), v);
         }
-        if (lane == 0) { s_rs[warp] = ws; s_ri[warp] = wi; }
+        // log-sum-exp of the row
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float om = __shfl_xor_sync(0xffffffffu, m, o);
+            const float os = __shfl_xor_sync(0xffffffffu, sum, o);
+            const float nm = fmaxf(m, om);
+            sum = (nm == -INFINITY) ? 0.f : sum * exp2f(m - nm) + os * exp2f(om - nm);
+            m = nm;
+        }
+        if (lane == 0) s_red[warp] = make_float2(m, sum);
         __syncthreads();
         if (tid == 0) {
-            float fs = s_rs[0];
-            int fi = s_ri[0];
-            for (int k = 1; k < kThreads / 32; ++k)
-                if (before(s_rs[k], s_ri[k], fs, fi)) { fs = s_rs[k]; fi = s_ri[k]; }
-            s_win[r] = fs;
-            s_wi[r] = fi;
+            float M = -INFINITY, S = 0.f;
+            for (int q = 0; q < kWarps; ++q) {
+                const float nm = fmaxf(M, s_red[q].x);
+                S = (nm == -INFINITY) ? 0.f : S * exp2f(M - nm) + s_red[q].y * exp2f(s_red[q].x - nm);
+                M = nm;
+            }
+            out.lse = (M + log2f(S)) * kLn2;
+        }
+        // the row's W best tokens
+        select(ls, li);
+        if (tid < W) {
+            out.val[tid] = s_win[tid];
+            out.tok[tid] = s_wi[tid];
         }
         __syncthreads();
-        if (bi != kNoIndex && bi == s_wi[r]) ++head;   // the owner of the winner advances
-        __syncthreads();
     }
-    // ---- outputs ------------------------------------------------------------
-    for (int k = tid; k < W * (t + 1); k += kThreads) {
-        const int r = k / (t + 1), pos = k % (t + 1);
-        const int fi = s_wi[r];
-        const bool ok = fi != kNoIndex;
-        const int pw = ok ? fi / V : 0, tok = ok ? fi % V : -1;
-        beams_out[((size_t)b * W + r) * (t + 1) + pos] =
-            pos < t ? (ok ? beams_in[((size_t)b * W + pw) * t + pos] : -1) : tok;
-        if (pos == 0) {
-            scores_out[(size_t)b * W + r] = s_win[r];
-            parent[(size_t)b * W + r] = ok ? pw : -1;
-            if (!ok) rd_flag(dev_status, RD_DEV_BAD_LENGTH);
+    cl.sync();                                   // every row published
+
+    // ---- rank 0: the request's W best candidates -------------------------------
+    if (rank == 0) {
+        float ls[W];
+        int li[W];
+#pragma unroll
+        for (int q = 0; q < W; ++q) { ls[q] = -INFINITY; li[q] = kNoIndex; }
+        if (tid < W * W) {                           // candidate (row w, its q-th best)
+            const int w = tid / W, q = tid % W;
+            const RowOut<W>* ro = cl.map_shared_rank(&s_row[w / C], w % C);
+            const float lse = ro->lse;
+            const int tok = ro->tok[q];
+            if (lse != -INFINITY && tok != kNoIndex) {
+                ls[0] = scores_in[(size_t)b * W + w] + (ro->val[q] - lse);
+                li[0] = w * V + tok;
+            }
+        }
+        select(ls, li);
+        for (int k = tid; k < W * (t + 1); k += kThreads) {
+            const int r = k / (t + 1), pos = k % (t + 1);
+            const int fi = s_wi[r];
+            const bool ok = fi != kNoIndex && s_win[r] != -INFINITY;
+            const int pw = ok ? fi / V : 0, tok = ok ? fi % V : -1;
+            beams_out[((size_t)b * W + r) * (t + 1) + pos] =
+                pos < t ? (ok ? beams_in[((size_t)b * W + pw) * t + pos] : -1) : tok;
+            if (pos == 0) {
+                scores_out[(size_t)b * W + r] = ok ? s_win[r] : -INFINITY;
+                parent[(size_t)b * W + r] = ok ? pw : -1;
+                if (!ok) rd_flag(dev_status, RD_DEV_BAD_LENGTH);
+            }
         }
     }
+    cl.sync();                                   // rank 0 is done reading its peers
 }
 
 }  // namespace
@@ -153,12 +220,22 @@ cudaError_t rd_launch_beam_step(const void* logits, const float* scores_in,
                                 int32_t* dev_status, cudaStream_t stream)
 {
     const uint16_t* lg = static_cast<const uint16_t*>(logits);
+    const int C = W < kMaxCluster ? W : kMaxCluster;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(B * C));
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
 #define RD_BEAM_CASE(WW)                                                                     \
     case WW:                                                                                 \
-        beam_step_kernel<WW><<<B, kThreads, 0, stream>>>(lg, scores_in, beams_in, V, t,      \
-                                                         beams_out, scores_out, parent,      \
-                                                         dev_status);                        \
-        break;
+        return cudaLaunchKernelEx(&cfg, beam_step_kernel<WW>, lg, scores_in, beams_in, V, t, \
+                                  beams_out, scores_out, parent, dev_status);
     switch (W) {
         RD_BEAM_CASE(1) RD_BEAM_CASE(2) RD_BEAM_CASE(3) RD_BEAM_CASE(4) RD_BEAM_CASE(5)
         RD_BEAM_CASE(6) RD_BEAM_CASE(7) RD_BEAM_CASE(8) RD_BEAM_CASE(9) RD_BEAM_CASE(10)
@@ -167,5 +244,4 @@ cudaError_t rd_launch_beam_step(const void* logits, const float* scores_in,
     default: return cudaErrorInvalidValue;
     }
 #undef RD_BEAM_CASE
-    return cudaGetLastError();
 }
