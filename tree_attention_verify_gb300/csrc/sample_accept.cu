@@ -39,6 +39,12 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
+// Bring [p, p + bytes) into L2 ahead of use (16-byte aligned start and size).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ float bf16_at(const uint16_t* row, int v)
 {
     return __uint_as_float(((uint32_t)__ldg(row + v)) << 16);
@@ -88,7 +94,7 @@ __device__ __forceinline__ KeyIdx ki_min(KeyIdx a, KeyIdx b)
 // (two slots, alternating, so a slot is rewritten only after every peer has
 // passed the next cluster barrier) and the warp partials.
 struct Scratch {
-    float4 pub[2];
+    float4 pub[2][kMaxCluster];    // [slot][rank of the writer]
     float4 warp[kWarps];
 };
 
@@ -111,15 +117,18 @@ __device__ float4 cluster_reduce(float4 x, Scratch& sc, int& slot, const cg::clu
     __syncthreads();                        // the previous reduction's readers are done
     if ((threadIdx.x & 31) == 0) sc.warp[threadIdx.x >> 5] = x;
     __syncthreads();
-    if (threadIdx.x == 0) {
+    const int n = (int)cl.num_blocks();
+    if (threadIdx.x < 32) {
+        // every lane folds the warp partials; lane i < n stores the result into
+        // CTA i of the cluster (a remote store, so the barrier below is the only
+        // wait and every CTA then reads its own shared memory)
         float4 r = sc.warp[0];
         for (int i = 1; i < kWarps; ++i) r = op(r, sc.warp[i]);
-        sc.pub[slot] = r;
+        if ((int)threadIdx.x < n) *cl.map_shared_rank(&sc.pub[slot][cl.block_rank()], threadIdx.x) = r;
     }
     cl.sync();
-    const int n = (int)cl.num_blocks();
-    float4 r = *cl.map_shared_rank(&sc.pub[slot], 0);
-    for (int i = 1; i < n; ++i) r = op(r, *cl.map_shared_rank(&sc.pub[slot], i));
+    float4 r = sc.pub[slot][0];
+    for (int i = 1; i < n; ++i) r = op(r, sc.pub[slot][i]);
     slot ^= 1;
     return r;
 }
@@ -182,6 +191,9 @@ sample_accept_kernel(const uint16_t* __restrict__ target, const uint16_t* __rest
     __shared__ int s_out[RD_MAX_PACKED + 1];
     __shared__ float s_invz[RD_MAX_BEAMS + 1];
     __shared__ float s_lz[RD_MAX_BEAMS + 1];
+    __shared__ int s_kid[RD_MAX_PACKED];         // children of the current node, in order
+    __shared__ float s_kt[RD_MAX_PACKED], s_kd[RD_MAX_PACKED], s_ku[RD_MAX_PACKED];
+    __shared__ int s_nkid;
     __shared__ Scratch sc;
     __shared__ int s_best;
 
@@ -237,6 +249,21 @@ sample_accept_kernel(const uint16_t* __restrict__ target, const uint16_t* __rest
 
     const float* ua = u_accept + (size_t)b * P_max;
     const float* us = u_sample + (size_t)b * V;
+    // the walk most often follows beam 0 (its nodes come first among every
+    // node's children): bring that path's rows of this CTA's slice into L2
+    {
+        const uint32_t bytes = (uint32_t)((v1 - v0) & ~7) * 2u;
+        const bool aligned = V % 8 == 0 && reinterpret_cast<uintptr_t>(target) % 16 == 0 &&
+                             reinterpret_cast<uintptr_t>(draft) % 16 == 0;
+        if (tid < L && aligned && bytes >= 16) {
+            const int nd = __ldg(up + tid);
+            if (nd >= 0 && nd < Pb) {
+                const size_t off = ((size_t)b * P_max + nd) * V + v0;
+                prefetch_l2(target + off, bytes);
+                prefetch_l2(draft + off, bytes);
+            }
+        }
+    }
     int slot = 0;
     int node = 0, a = 0;
     if (tid == 0) s_walk[0] = 0;
@@ -245,13 +272,43 @@ sample_accept_kernel(const uint16_t* __restrict__ target, const uint16_t* __rest
         const uint16_t* dr = draft + ((size_t)b * P_max + node) * V;
         const bool vec = (V % 8 == 0) && (reinterpret_cast<uintptr_t>(tr) % 16 == 0) &&
                          (reinterpret_cast<uintptr_t>(dr) % 16 == 0);
+        // ---- children of this node: their tokens' logits and uniforms, read now
+        // so that their latency overlaps pass 1; the first child's rows (the
+        // likeliest next node) are prefetched into L2 --------------------------
+        __syncthreads();                      // the previous node's reads are done
+        if (tid < 32) {                       // children in packed order, by ballot
+            int nk = 0;
+            for (int c0 = node + 1; c0 < Pb; c0 += 32) {
+                const int c = c0 + (int)tid;
+                const bool kid = c < Pb && s_parent[c] == node && s_token[c] >= 0;
+                const unsigned m = __ballot_sync(0xffffffffu, kid);
+                if (kid) s_kid[nk + __popc(m & ((1u << tid) - 1u))] = c;
+                nk += __popc(m);
+            }
+            if (tid == 0) {
+                s_nkid = nk;
+                const uint32_t bytes = (uint32_t)((v1 - v0) & ~7) * 2u;
+                if (nk > 0 && vec && bytes >= 16) {
+                    const size_t off = ((size_t)b * P_max + s_kid[0]) * V + v0;
+                    prefetch_l2(target + off, bytes);
+                    prefetch_l2(draft + off, bytes);
+                }
+            }
+        }
+        __syncthreads();
+        const int nkid = s_nkid;
+        for (int i = tid; i < nkid; i += kThreads) {
+            const int c = s_kid[i], x = s_token[c];
+            s_kt[i] = bf16_at(tr, x);
+            s_kd[i] = bf16_at(dr, x);
+            s_ku[i] = __ldg(ua + c);
+        }
         // ---- pass 1: softmax maxima and sums of both rows (log2 units) --------
         MaxSum mt{-INFINITY, 0.f}, md{-INFINITY, 0.f};
         if (vec) {
             const uint4* t4 = reinterpret_cast<const uint4*>(tr);
             const uint4* d4 = reinterpret_cast<const uint4*>(dr);
-            for (int i = (v0 >> 3) + tid; i < (v1 >> 3); i += kThreads) {
-                const uint4 ta = __ldg(t4 + i), da = __ldg(d4 + i);
+            auto fold = [&](const uint4& ta, const uint4& da) {
                 const uint32_t tw[4] = {ta.x, ta.y, ta.z, ta.w}, dw[4] = {da.x, da.y, da.z, da.w};
                 float xt[8], xd[8];
 #pragma unroll
@@ -263,6 +320,15 @@ sample_accept_kernel(const uint16_t* __restrict__ target, const uint16_t* __rest
                 }
                 ms_add8(mt, xt);
                 ms_add8(md, xd);
+            };
+            const int i1 = v1 >> 3;
+            for (int i = (v0 >> 3) + tid; i < i1; i += 2 * kThreads) {
+                const bool two = i + kThreads < i1;      // both loads issued before use
+                const uint4 ta = __ldg(t4 + i), da = __ldg(d4 + i);
+                uint4 tb = make_uint4(0, 0, 0, 0), db = tb;
+                if (two) { tb = __ldg(t4 + i + kThreads); db = __ldg(d4 + i + kThreads); }
+                fold(ta, da);
+                if (two) fold(tb, db);
             }
         } else {
             for_each_pair(tr, dr, v0, v1, false, [&](int, float t, float d) {
@@ -284,18 +350,16 @@ sample_accept_kernel(const uint16_t* __restrict__ target, const uint16_t* __rest
         };
         // ---- children in packed order -----------------------------------------
         int k = 0, accepted = -1;
-        for (int c = node + 1; c < Pb; ++c) {
-            if (s_parent[c] != node) continue;
-            const int x = s_token[c];
-            if (x < 0) continue;
+        for (int i = 0; i < nkid; ++i) {
+            const int c = s_kid[i];
             // u q(x) < R_k(x), on log2 values
-            const float lq = bf16_at(dr, x) * c2 - md.m - lsd;
-            float lr = bf16_at(tr, x) * c2 - mt.m - lst;
+            const float lq = s_kd[i] * c2 - md.m - lsd;
+            float lr = s_kt[i] * c2 - mt.m - lst;
             for (int j = 0; j < k; ++j) {
                 if (s_invz[j] > 0.f)
                     lr = (lr > lq) ? lr + __log2f(-expm1f((lq - lr) * kLn2)) - s_lz[j] : -INFINITY;
             }
-            const float u = __ldg(ua + c);
+            const float u = s_ku[i];
             const float lu = u > 0.f ? __log2f(u) : -INFINITY;
             if (lu + lq < lr) { accepted = c; break; }
             // rejected: mass of the next residual
@@ -344,8 +408,13 @@ sample_accept_kernel(const uint16_t* __restrict__ target, const uint16_t* __rest
         }
         __syncthreads();
         for (int w = tid; w < W; w += kThreads) {
+            // leading positions of beam w on the walk (loads issued independently)
             int n = -1;
-            while (n + 1 <= a && n + 1 < L && __ldg(up + w * L + n + 1) == s_walk[n + 1]) ++n;
+            bool on = true;
+            for (int j = 0; j <= a && j < L; ++j) {
+                on = on && __ldg(up + w * L + j) == s_walk[j];
+                if (on) n = j;
+            }
             accept_len[(size_t)b * W + w] = n < 0 ? 0 : n;
             if (n == a) atomicMin(&s_best, w);
         }
