@@ -276,6 +276,56 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, ok);
 }
 
+// Combine the split partials of one output row:
+// out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s, 64 columns at a time with
+// the 16 loads of a split's part in flight together.  Kept out of line: it runs
+// once per row and unit, and inlining it into the kernel body slowed the
+// streaming loop of the single-split case.
+template <int D>
+__device__ __noinline__ void merge_split_row(const TcArgs& a, size_t prow, int n_splits,
+                                             bool valid, uint16_t* dst)
+{
+    const float2* mlp = a.ml_part + prow * a.splits;
+    const float* opp = a.o_part + prow * a.splits * D;
+    float M = -INFINITY;
+    for (int sp = 0; sp < n_splits; ++sp) M = fmaxf(M, __ldcg(&mlp[sp].x));
+    const bool any = valid && M != -INFINITY;
+    float Ls = 0.f, inv = 0.f;
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h) {
+        float acc[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) acc[c] = 0.f;
+        for (int sp = 0; any && sp < n_splits; ++sp) {
+            const float2 ml = __ldcg(&mlp[sp]);
+            if (ml.x == -INFINITY) continue;
+            const float w = exp2f(ml.x - M);
+            if (h == 0) Ls += ml.y * w;
+            const float4* src = reinterpret_cast<const float4*>(opp + (size_t)sp * D + h * 64);
+            float4 x[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) x[i] = __ldcg(src + i);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                acc[4 * i + 0] += x[i].x * w;
+                acc[4 * i + 1] += x[i].y * w;
+                acc[4 * i + 2] += x[i].z * w;
+                acc[4 * i + 3] += x[i].w * w;
+            }
+        }
+        if (h == 0) inv = (any && Ls > 0.f) ? a.out_scale / Ls : 0.f;
+#pragma unroll
+        for (int c = 0; c < 64; c += 8) {
+            uint4 v;
+            v.x = pack_bf16(acc[c + 0] * inv, acc[c + 1] * inv);
+            v.y = pack_bf16(acc[c + 2] * inv, acc[c + 3] * inv);
+            v.z = pack_bf16(acc[c + 4] * inv, acc[c + 5] * inv);
+            v.w = pack_bf16(acc[c + 6] * inv, acc[c + 7] * inv);
+            *reinterpret_cast<uint4*>(dst + h * 64 + c) = v;
+        }
+    }
+}
+
 template <int D, bool F8>
 __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
 tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map_kc,
@@ -938,40 +988,9 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 if (s_last) {
                     __threadfence();
                     const int p = row / a.G;
-                    if (p < a.P_max) {
-                        float M = -INFINITY;
-                        for (int sp = 0; sp < geo.n_splits; ++sp)
-                            M = fmaxf(M, __ldcg(&a.ml_part[prow * a.splits + sp].x));
-                        float wsum[8];
-                        int nw = 0;
-                        float Ls = 0.f;
-                        (void)wsum; (void)nw;
-                        uint16_t* dst = a.o + (((size_t)geo.b * a.P_max + p) * a.Hq + hq0 + row % a.G) * D;
-                        for (int c = 0; c < D; c += 8) {
-                            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                            Ls = 0.f;
-                            if (valid && M != -INFINITY) {
-                                for (int sp = 0; sp < geo.n_splits; ++sp) {
-                                    const float2 ml = __ldcg(&a.ml_part[prow * a.splits + sp]);
-                                    if (ml.x == -INFINITY) continue;
-                                    const float w = exp2f(ml.x - M);
-                                    Ls += ml.y * w;
-                                    const float* src = a.o_part + (prow * a.splits + sp) * D + c;
-                                    const float4 x0 = __ldcg(reinterpret_cast<const float4*>(src));
-                                    const float4 x1 = __ldcg(reinterpret_cast<const float4*>(src + 4));
-                                    acc[0] += x0.x * w; acc[1] += x0.y * w; acc[2] += x0.z * w; acc[3] += x0.w * w;
-                                    acc[4] += x1.x * w; acc[5] += x1.y * w; acc[6] += x1.z * w; acc[7] += x1.w * w;
-                                }
-                            }
-                            const float inv = (valid && Ls > 0.f) ? a.out_scale / Ls : 0.f;
-                            uint4 v;
-                            v.x = pack_bf16(acc[0] * inv, acc[1] * inv);
-                            v.y = pack_bf16(acc[2] * inv, acc[3] * inv);
-                            v.z = pack_bf16(acc[4] * inv, acc[5] * inv);
-                            v.w = pack_bf16(acc[6] * inv, acc[7] * inv);
-                            *reinterpret_cast<uint4*>(dst + c) = v;
-                        }
-                    }
+                    if (p < a.P_max)
+                        merge_split_row<D>(a, prow, geo.n_splits, valid,
+                                           a.o + (((size_t)geo.b * a.P_max + p) * a.Hq + hq0 + row % a.G) * D);
                     if (t == 0) a.tickets[unit_id] = 0u;
                 }
             }
