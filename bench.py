@@ -51,7 +51,7 @@ def _args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="13b_b64", choices=list(workloads.CONFIGS))
-    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-sample-requests", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -338,6 +338,67 @@ def measure_next_rows(cfg, inp, step, dev, peak: float) -> dict:
     return rows
 
 
+def _peak_tflops():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def measure_mixed(dev) -> dict:
+    """The in-flight batch on 8B-GQA shapes (32 requests, each a 512-token causal
+    prefill chunk with probability 0.5, else a W=8, L=5 verification over a
+    512-8192 context) and its all-context / all-generation splits: one in-flight
+    step = causal attention + next-token argmax of the context half, and
+    pack + tree attention + greedy accept + unpack of the generation half."""
+    import tree_attention_verify_gb300 as rd
+    from tree_attention_verify_gb300.step import VerifyStep
+    peak_tf, _ = _peak_tflops()
+    out = {}
+    for split in ("mixed", "all_ctx", "all_gen"):
+        m = workloads.make_mixed_inputs(split, device=dev)
+        c, g = m["ctx"], m["gen"]
+        n_ctx, n_gen, T = m["n_ctx"], m["n_gen"], m["prefill_len"]
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        parts = []
+        row = {"n_context": n_ctx, "n_generation": n_gen}
+        if n_ctx:
+            oc = torch.empty_like(c["q"])
+            one = torch.zeros((n_ctx, 1, 1), dtype=torch.int32, device=dev)
+            plen1 = torch.ones(n_ctx, dtype=torch.int32, device=dev)
+            V = c["logits"].shape[2]
+            wsc = torch.zeros(max(8, rd.rd_greedy_accept_workspace_size(n_ctx, 1, V)),
+                              dtype=torch.uint8, device=dev)
+            accc = rd.rd_greedy_accept(c["logits"], one, one, plen1, workspace=wsc, dev_status=st)
+            causal = lambda: rd.rd_causal_attention(c["q"], c["k"], c["v"], c["cu_seqlens"],  # noqa
+                                                    max_seqlen=T, out=oc, dev_status=st)
+            parts.append(causal)
+            parts.append(lambda: rd.rd_greedy_accept(c["logits"], one, one, plen1, out=accc,
+                                                     workspace=wsc, dev_status=st))
+            Hq, D = c["q"].shape[1], c["q"].shape[2]
+            flops = float(sum(4.0 * Hq * D * t * (t + 1) / 2 for t in c["seq_lens"]))
+            us = _time_us(causal)
+            row["rd_causal_attention"] = {"us": us, "tflops": flops / us / 1e6,
+                                          "frac": flops / us / 1e6 / peak_tf,
+                                          "bound": "tensor"}
+        if n_gen:
+            gc = g["cfg"]
+            step = VerifyStep(gc.B, gc.W, gc.L, gc.Hq, gc.Hkv, gc.D, gc.vocab, gc.Dh,
+                              max(1, int(g["ctx_lens"].max())), dev)
+            parts.append(lambda: step(g["beams"], g["q"], g["k_draft"], g["v_draft"],
+                                      g["k_cache"], g["v_cache"], g["ctx_offsets"], g["logits"],
+                                      g["hidden"]))
+        us = _time_us(lambda: [f() for f in parts])
+        row["step_us"] = us
+        row["requests_per_s"] = (n_ctx + n_gen) / us * 1e6
+        torch.cuda.synchronize()
+        if int(st.item()) != 0:
+            raise SystemExit(f"device status {int(st.item())} in the in-flight batch")
+        out[split] = row
+    return out
+
+
 def run_ours(args):
     import tree_attention_verify_gb300 as rd
     from tree_attention_verify_gb300.step import VerifyStep
@@ -410,6 +471,7 @@ def run_ours(args):
     next_rows = None
     if rank == 0 and not args.no_next_rows:
         next_rows = measure_next_rows(cfg, inp, step, dev, peak)
+        next_rows["inflight_batch_8b"] = measure_mixed(dev)
 
     # ---- end to end through the public API, host buffers ----------------------
     # Every step copies its inputs from pinned host memory and reads its accepted
@@ -433,16 +495,11 @@ def run_ours(args):
         done = [torch.cuda.Event() for _ in range(2)]
 
         def e2e_run(n_steps):
+            # iteration k: enqueue step k-1 first (its inputs were copied in
+            # iteration k-1), so the compute stream never waits for the host;
+            # then wait until step k-2 has finished (its buffers are free) and
+            # enqueue the copies of step k
             for k in range(n_steps + 1):
-                if k < n_steps:
-                    sb = k % 2
-                    if k >= 2:
-                        done[sb].synchronize()            # result k-2 read back, buffers free
-                    copy_stream.wait_event(consumed[sb])
-                    with torch.cuda.stream(copy_stream):
-                        for n in names:
-                            devbuf[sb][n].copy_(host[n], non_blocking=True)
-                        copied[sb].record(copy_stream)
                 if k >= 1:
                     j = k - 1
                     sb = j % 2
@@ -454,6 +511,15 @@ def run_ours(args):
                     for n in outs:
                         host_out[sb][n].copy_(step.acc[n], non_blocking=True)
                     done[sb].record(stream)
+                if k < n_steps:
+                    sb = k % 2
+                    if k >= 2:
+                        done[sb].synchronize()            # result k-2 read back, buffers free
+                    copy_stream.wait_event(consumed[sb])
+                    with torch.cuda.stream(copy_stream):
+                        for n in names:
+                            devbuf[sb][n].copy_(host[n], non_blocking=True)
+                        copied[sb].record(copy_stream)
             for e in done:
                 e.synchronize()
 
