@@ -105,3 +105,10 @@ def test_fp8_unsupported_shapes_are_rejected():
         q2 = torch.zeros((1, 4, 2, 128), dtype=torch.bfloat16, device=DEV)
         kc2 = torch.zeros((8, 2, 128), dtype=torch.uint8, device=DEV)
         rd.rd_tree_attention_fp8(q2, q2, q2, kc2, kc2, 0.0, 1.0, offs, pl, mask, max_ctx=8)
+
+
+def test_fp8_maximum_packed_length():
+    cfg = dataclasses.replace(workloads.CONFIGS["tiny"], B=2, W=32, L=8, vocab=100000, Hq=4,
+                              Hkv=2, D=128, share=("p", 0.05), ctx=("uniform", 1, 300),
+                              ties=False)
+    _fp8_case(cfg)

@@ -408,3 +408,16 @@ def test_tree_attention_growing_scores_rescale():
     inp["k_cache"] = (ramp * torch.ones(1, 1, cfg.D)).to(torch.bfloat16).contiguous()
     inp["q"] = torch.full_like(inp["q"], 1.0)
     _attention_case(inp)
+
+
+def test_tree_attention_maximum_packed_length():
+    # W*L = 256 packed nodes (the largest P_max), 8 mask words, 4 draft chunks,
+    # G = 2 -> 512 stacked rows = 4 tiles per (request, kv head)
+    import dataclasses
+    cfg = dataclasses.replace(workloads.CONFIGS["tiny"], B=2, W=32, L=8, vocab=100000, Hq=4,
+                              Hkv=2, D=128, share=("p", 0.05), ctx=("uniform", 1, 300),
+                              ties=False)
+    inp = workloads.make_verify_inputs(cfg, device="cpu")
+    pk = oracle.oracle_pack(inp["beams"].numpy(), cfg.P_max)
+    assert pk["packed_len"].max() > 192              # the last draft chunk is used
+    _attention_case(inp)
