@@ -134,14 +134,26 @@ beam_step_kernel(const uint16_t* __restrict__ logits, const float* __restrict__ 
         };
         const bool vec = (V % 8 == 0) && (reinterpret_cast<uintptr_t>(row) % 16 == 0);
         if (vec) {
+            // four 16-byte loads in flight per thread before any of them is used
             const uint4* r4 = reinterpret_cast<const uint4*>(row);
-            for (int i = tid; i < V / 8; i += kThreads) {
-                const uint4 x = __ldg(r4 + i);
-                const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+            const int n4 = V / 8;
+            for (int base = tid; base < n4; base += 4 * kThreads) {
+                uint4 x[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    take(__uint_as_float(xw[e] << 16), i * 8 + 2 * e);
-                    take(__uint_as_float(xw[e] & 0xffff0000u), i * 8 + 2 * e + 1);
+                for (int q = 0; q < 4; ++q) {
+                    const int i = base + q * kThreads;
+                    x[q] = i < n4 ? __ldg(r4 + i) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int i = base + q * kThreads;
+                    if (i >= n4) break;
+                    const uint32_t xw[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        take(__uint_as_float(xw[e] << 16), i * 8 + 2 * e);
+                        take(__uint_as_float(xw[e] & 0xffff0000u), i * 8 + 2 * e + 1);
+                    }
                 }
             }
         } else {

@@ -157,16 +157,30 @@ __device__ __forceinline__ void for_each_pair(const uint16_t* tr, const uint16_t
                                               int v1, bool vec, F&& f)
 {
     if (vec) {
+        // two 16-byte loads per row in flight per thread before any is used
         const uint4* t4 = reinterpret_cast<const uint4*>(tr);
         const uint4* d4 = reinterpret_cast<const uint4*>(dr);
-        for (int i = (v0 >> 3) + (int)threadIdx.x; i < (v1 >> 3); i += kThreads) {
-            const uint4 a = __ldg(t4 + i), c = __ldg(d4 + i);
-            const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, cw[4] = {c.x, c.y, c.z, c.w};
+        const int i1 = v1 >> 3;
+        for (int base = (v0 >> 3) + (int)threadIdx.x; base < i1; base += 2 * kThreads) {
+            uint4 a[2], c[2];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                f(i * 8 + 2 * e, __uint_as_float(aw[e] << 16), __uint_as_float(cw[e] << 16));
-                f(i * 8 + 2 * e + 1, __uint_as_float(aw[e] & 0xffff0000u),
-                  __uint_as_float(cw[e] & 0xffff0000u));
+            for (int q = 0; q < 2; ++q) {
+                const int i = base + q * kThreads;
+                a[q] = i < i1 ? __ldg(t4 + i) : make_uint4(0, 0, 0, 0);
+                c[q] = i < i1 ? __ldg(d4 + i) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int i = base + q * kThreads;
+                if (i >= i1) break;
+                const uint32_t aw[4] = {a[q].x, a[q].y, a[q].z, a[q].w};
+                const uint32_t cw[4] = {c[q].x, c[q].y, c[q].z, c[q].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    f(i * 8 + 2 * e, __uint_as_float(aw[e] << 16), __uint_as_float(cw[e] << 16));
+                    f(i * 8 + 2 * e + 1, __uint_as_float(aw[e] & 0xffff0000u),
+                      __uint_as_float(cw[e] & 0xffff0000u));
+                }
             }
         }
     } else {
