@@ -86,13 +86,16 @@ beam_step_kernel(const uint16_t* __restrict__ logits, const float* __restrict__ 
             }
             if (lane == 0) { s_rs[warp] = ws; s_ri[warp] = wi; }
             __syncthreads();
-            if (tid == 0) {
-                float fs = s_rs[0];
-                int fi = s_ri[0];
-                for (int k = 1; k < kWarps; ++k)
-                    if (before(s_rs[k], s_ri[k], fs, fi)) { fs = s_rs[k]; fi = s_ri[k]; }
-                s_win[r] = fs;
-                s_wi[r] = fi;
+            if (warp == 0) {                     // the warps' winners, by shuffles
+                float fs = lane < kWarps ? s_rs[lane] : -INFINITY;
+                int fi = lane < kWarps ? s_ri[lane] : kNoIndex;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float os = __shfl_xor_sync(0xffffffffu, fs, o);
+                    const int oi = __shfl_xor_sync(0xffffffffu, fi, o);
+                    if (before(os, oi, fs, fi)) { fs = os; fi = oi; }
+                }
+                if (lane == 0) { s_win[r] = fs; s_wi[r] = fi; }
             }
             __syncthreads();
             if (bi != kNoIndex && bi == s_wi[r]) ++head;   // the owner of the winner advances
