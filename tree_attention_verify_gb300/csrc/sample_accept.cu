@@ -442,9 +442,11 @@ sample_accept_kernel(const uint16_t* __restrict__ target, const uint16_t* __rest
 
 int rd_sample_cluster_size(int B)
 {
-    // enough CTAs to cover the SMs about twice, at most kMaxCluster per request
+    // enough CTAs to cover the SMs once, at most kMaxCluster per request (a
+    // sweep at B = 64 / 16 / 1 found 4 / 8 / 4-8 CTAs per request fastest:
+    // more CTAs add cluster-barrier cost to every pass, fewer add pass length)
     int c = 1;
-    while (c < kMaxCluster && (long)B * c < 2L * 152) c *= 2;
+    while (c < kMaxCluster && (long)B * c < 152) c *= 2;
     return c;
 }
 
