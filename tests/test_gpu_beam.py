@@ -85,3 +85,20 @@ def test_beam_search_drafts_then_pack():
     pk = rd.rd_pack_beams(beams.contiguous(), W * L)
     ref = oracle.oracle_pack(beams.cpu().numpy(), W * L)
     np.testing.assert_array_equal(pk["packed_len"].cpu().numpy(), ref["packed_len"])
+
+
+def test_beam_search_step_all_tied_rows():
+    # every logit of a row equal: more tied candidates than the kernel's
+    # candidate slots, which exercises its exact fallback selection
+    import tree_attention_verify_gb300 as rd
+    B, W, V, t = 3, 4, 5000, 2
+    lg = torch.zeros((B, W, V), dtype=torch.bfloat16, device=DEV)
+    lg[1, 2, 4000:] = 1.0                        # one row with a tied block at the top
+    g = torch.Generator(device=DEV).manual_seed(7)
+    s_in = torch.randn(B, W, generator=g, device=DEV)
+    beams_in = torch.randint(0, 1000, (B, W, t), generator=g, device=DEV, dtype=torch.int32)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = rd.rd_beam_search_step(lg, s_in, beams_in, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    _check(lg, s_in, beams_in, got)

@@ -29,6 +29,7 @@ constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kNoIndex = 0x7fffffff;
 constexpr int kMaxCluster = 8;
+constexpr int kCap = 1024;                 // candidate slots per row
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -59,6 +60,9 @@ beam_step_kernel(const uint16_t* __restrict__ logits, const float* __restrict__ 
     __shared__ int s_ri[kWarps];
     __shared__ float s_win[W];
     __shared__ int s_wi[W];
+    __shared__ float s_cv[kCap];          // candidates of a row: logit and token
+    __shared__ int s_ci[kCap];
+    __shared__ int s_cnt;
 
     const cg::cluster_group cl = cg::this_cluster();
     const int C = (int)cl.num_blocks();
@@ -113,57 +117,47 @@ beam_step_kernel(const uint16_t* __restrict__ logits, const float* __restrict__ 
             continue;
         }
         const uint16_t* row = logits + ((size_t)b * W + w) * V;
-        float m = -INFINITY, sum = 0.f;          // log2 units
-        float ls[W];
-        int li[W];
+        const bool vec = (V % 8 == 0) && (reinterpret_cast<uintptr_t>(row) % 16 == 0);
+        // visit every token of the row: f(logit, token), four 16-byte loads in
+        // flight per thread before any of them is used
+        auto for_row = [&](auto&& f) {
+            if (vec) {
+                const uint4* r4 = reinterpret_cast<const uint4*>(row);
+                const int n4 = V / 8;
+                for (int base = tid; base < n4; base += 4 * kThreads) {
+                    uint4 x[4];
 #pragma unroll
-        for (int q = 0; q < W; ++q) { ls[q] = -INFINITY; li[q] = kNoIndex; }
-        auto take = [&](float x, int v) {
+                    for (int q = 0; q < 4; ++q) {
+                        const int i = base + q * kThreads;
+                        x[q] = i < n4 ? __ldg(r4 + i) : make_uint4(0, 0, 0, 0);
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int i = base + q * kThreads;
+                        if (i >= n4) break;
+                        const uint32_t xw[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            f(__uint_as_float(xw[e] << 16), i * 8 + 2 * e);
+                            f(__uint_as_float(xw[e] & 0xffff0000u), i * 8 + 2 * e + 1);
+                        }
+                    }
+                }
+            } else {
+                for (int v = tid; v < V; v += kThreads)
+                    f(__uint_as_float((uint32_t)__ldg(row + v) << 16), v);
+            }
+        };
+        // ---- pass 1: log-sum-exp and every thread's best token ----------------
+        float m = -INFINITY, sum = 0.f;          // log2 units
+        float bv = -INFINITY;
+        int bi = kNoIndex;
+        for_row([&](float x, int v) {
             const float y = x * kLog2e;
             if (y > m) { sum = (m == -INFINITY) ? 0.f : sum * exp2f(m - y); m = y; }
             if (y != -INFINITY) sum += exp2f(y - m);
-            if (!before(x, v, ls[W - 1], li[W - 1])) return;
-            float cs = x;
-            int ci = v;
-#pragma unroll
-            for (int q = 0; q < W; ++q) {        // insert into the sorted list
-                if (before(cs, ci, ls[q], li[q])) {
-                    const float ts = ls[q];
-                    const int ti = li[q];
-                    ls[q] = cs; li[q] = ci;
-                    cs = ts; ci = ti;
-                }
-            }
-        };
-        const bool vec = (V % 8 == 0) && (reinterpret_cast<uintptr_t>(row) % 16 == 0);
-        if (vec) {
-            // four 16-byte loads in flight per thread before any of them is used
-            const uint4* r4 = reinterpret_cast<const uint4*>(row);
-            const int n4 = V / 8;
-            for (int base = tid; base < n4; base += 4 * kThreads) {
-                uint4 x[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int i = base + q * kThreads;
-                    x[q] = i < n4 ? __ldg(r4 + i) : make_uint4(0, 0, 0, 0);
-                }
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int i = base + q * kThreads;
-                    if (i >= n4) break;
-                    const uint32_t xw[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        take(__uint_as_float(xw[e] << 16), i * 8 + 2 * e);
-                        take(__uint_as_float(xw[e] & 0xffff0000u), i * 8 + 2 * e + 1);
-                    }
-                }
-            }
-        } else {
-            for (int v = tid; v < V; v += kThreads)
-                take(__uint_as_float((uint32_t)__ldg(row + v) << 16), v);
-        }
-        // log-sum-exp of the row
+            if (before(x, v, bv, bi)) { bv = x; bi = v; }
+        });
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             const float om = __shfl_xor_sync(0xffffffffu, m, o);
@@ -172,8 +166,30 @@ beam_step_kernel(const uint16_t* __restrict__ logits, const float* __restrict__ 
             sum = (nm == -INFINITY) ? 0.f : sum * exp2f(m - nm) + os * exp2f(om - nm);
             m = nm;
         }
-        if (lane == 0) s_red[warp] = make_float2(m, sum);
+        // a threshold: the W-th best of a warp's 32 thread maxima.  At least W
+        // tokens of the row reach it, so every token of the row's top W does too
+        float tw = -INFINITY;
+        {
+            float cv = bv;
+            int ci = bi;
+            for (int r = 0; r < W; ++r) {
+                float ws = cv;
+                int wi = ci;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float os = __shfl_xor_sync(0xffffffffu, ws, o);
+                    const int oi = __shfl_xor_sync(0xffffffffu, wi, o);
+                    if (before(os, oi, ws, wi)) { ws = os; wi = oi; }
+                }
+                if (r == W - 1) tw = (wi == kNoIndex) ? -INFINITY : ws;
+                if (ci != kNoIndex && ci == wi) { cv = -INFINITY; ci = kNoIndex; }
+            }
+        }
+        if (lane == 0) { s_red[warp] = make_float2(m, sum); s_rs[warp] = tw; }
+        if (tid == 0) s_cnt = 0;
         __syncthreads();
+        float thr = -INFINITY;
+        for (int q = 0; q < kWarps; ++q) thr = fmaxf(thr, s_rs[q]);
         if (tid == 0) {
             float M = -INFINITY, S = 0.f;
             for (int q = 0; q < kWarps; ++q) {
@@ -183,11 +199,63 @@ beam_step_kernel(const uint16_t* __restrict__ logits, const float* __restrict__ 
             }
             out.lse = (M + log2f(S)) * kLn2;
         }
-        // the row's W best tokens
-        select(ls, li);
-        if (tid < W) {
-            out.val[tid] = s_win[tid];
-            out.tok[tid] = s_wi[tid];
+        // ---- pass 2: the tokens that reach the threshold (from L1/L2) -----------
+        for_row([&](float x, int v) {
+            if (x >= thr) {
+                const int k = atomicAdd(&s_cnt, 1);
+                if (k < kCap) { s_cv[k] = x; s_ci[k] = v; }
+            }
+        });
+        __syncthreads();
+        const int cnt = s_cnt;
+        if (cnt <= kCap) {
+            // the row's W best among the candidates, by one warp
+            if (warp == 0) {
+                for (int r = 0; r < W; ++r) {
+                    float ws = -INFINITY;
+                    int wi = kNoIndex, wk = -1;
+                    for (int q = lane; q < cnt; q += 32)
+                        if (s_ci[q] != kNoIndex && before(s_cv[q], s_ci[q], ws, wi)) {
+                            ws = s_cv[q]; wi = s_ci[q]; wk = q;
+                        }
+                    const int mine = wi;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        const float os = __shfl_xor_sync(0xffffffffu, ws, o);
+                        const int oi = __shfl_xor_sync(0xffffffffu, wi, o);
+                        if (before(os, oi, ws, wi)) { ws = os; wi = oi; }
+                    }
+                    if (lane == 0) { out.val[r] = ws; out.tok[r] = wi; }
+                    if (mine != kNoIndex && mine == wi) s_ci[wk] = kNoIndex;   // taken
+                    __syncwarp();
+                }
+            }
+        } else {
+            // more candidates than room (ties or -inf rows): every thread's best W,
+            // then W CTA-wide rounds
+            float ls[W];
+            int li[W];
+#pragma unroll
+            for (int q = 0; q < W; ++q) { ls[q] = -INFINITY; li[q] = kNoIndex; }
+            for_row([&](float x, int v) {
+                if (!before(x, v, ls[W - 1], li[W - 1])) return;
+                float cs = x;
+                int ci = v;
+#pragma unroll
+                for (int q = 0; q < W; ++q) {    // insert into the sorted list
+                    if (before(cs, ci, ls[q], li[q])) {
+                        const float ts = ls[q];
+                        const int ti = li[q];
+                        ls[q] = cs; li[q] = ci;
+                        cs = ts; ci = ti;
+                    }
+                }
+            });
+            select(ls, li);
+            if (tid < W) {
+                out.val[tid] = s_win[tid];
+                out.tok[tid] = s_wi[tid];
+            }
         }
         __syncthreads();
     }
