@@ -11,8 +11,8 @@
 // Work unit = (request b, kv head h, 128-row query tile, KV split).  The G query
 // heads that share kv head h are stacked as rows (row r -> node p = r / G, head
 // h*G + r % G; causal: token t = r / G), so each K/V byte is read once per tile.
-// Row r of a tile is TMEM lane r.  A unit walks its KV chunks (64 positions;
-// FP8: 128): first the context (all visible; the last chunk is ragged), then
+// Row r of a tile is TMEM lane r.  A unit walks its KV chunks (64 positions):
+// first the context (all visible; the last chunk is ragged), then
 // the packed drafts (visible iff the node's ancestor-mask bit is set).
 //
 // Warp roles (one CTA per SM, persistent over units):
@@ -27,12 +27,11 @@
 //   warp 6     PV issuer: O += P V (M=128, N=D, K=chunk; A = P in TMEM) into
 //              TMEM.  The two issuers run independently.
 // FP8 variant (template flag F8; context K/V stored as e4m3 with per-tensor
-// scales): 128-position chunks; the producer TMA-loads e4m3 context chunks
-// into an 8-bit ring; warps 6-9 widen them (exactly) into the 16-bit ring the
-// MMA reads, and convert the bf16 draft chunks, divided by the scales, the same
-// way; warp 5 issues both S and PV; P is written over the first half of its
-// chunk's S buffer.  The MMA runs kind::f16 with f16 operands (e4m3 widens to
-// f16 exactly and both operands of one MMA share a type); the K scale is
+// scales): the producer TMA-loads e4m3 context chunks into an 8-bit ring;
+// warps 6-9 widen them (exactly) into the 16-bit ring the MMA reads, and
+// convert the bf16 draft chunks, divided by the scales, the same way; warp 5
+// issues both S and PV.  The MMA runs kind::f16 with f16 operands (e4m3 widens to f16 exactly and both
+// operands of one MMA share a type); the K scale is
 // folded into the softmax scale and the V scale into the output normalisation.
 // Every wait is bounded by a clock budget; on expiry the CTA records
 // RD_DEV_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM and exits.
@@ -42,6 +41,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "rd_internal.cuh"
 #include "tc_ptx.cuh"
@@ -50,13 +50,12 @@ namespace {
 using namespace rdtc;
 
 constexpr int kM = 128;                    // query rows per tile = TMEM lanes
-constexpr int kN = 64;                     // KV positions per chunk (bf16)
-constexpr int kNF8 = 64;                   // KV positions per chunk (FP8)
+constexpr int kN = 64;                     // KV positions per chunk
 constexpr int kSoftmaxThreads = 128;
 constexpr int kThreads = kSoftmaxThreads + 96;          // + producer, S issuer, PV issuer
 constexpr int kThreadsF8 = kSoftmaxThreads + 64 + 128;  // + producer, MMA issuer, 4 converters
 constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;                // bf16: S issuer; FP8: S and PV issuer
+constexpr int kMmaWarp = 5;                // S issuer (FP8: S and PV) and TMEM owner
 constexpr int kPvWarp = 6;                 // bf16 only: PV issuer
 constexpr int kConvWarp0 = 6;              // FP8 only: first converter warp
 constexpr float kLog2e = 1.4426950408889634f;
@@ -64,20 +63,12 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when a max g
 constexpr long long kWaitBudget = 4000000000LL;   // ~2 s of SM clock per wait
 
 template <int D, bool F8 = false> struct Cfg {
-    static constexpr int kNc = F8 ? kNF8 : kN;         // KV positions per chunk
+    static constexpr int kNc = kN;                      // KV positions per chunk
     static constexpr int kDB = D / 64;                  // 64-element (128-byte) column blocks
     // 16-bit ring and (FP8) 8-bit ring of context chunks, 224 KB in all
-    static constexpr int kStages = F8 ? (kNc == 128 ? 2 : 5) : (D == 128 ? 7 : 8);
-    static constexpr int kF8Stages = F8 ? (kNc == 128 ? 3 : 4) : 0;
+    static constexpr int kStages = F8 ? 5 : (D == 128 ? 7 : 8);
+    static constexpr int kF8Stages = F8 ? 4 : 0;
     static constexpr int kF8Ring = kF8Stages > 0 ? kF8Stages : 1;   // ring index modulus
-    // converter warps writing each of K and V: 128-position chunks give every
-    // converter thread one K row and one V row; 64-position chunks give warps
-    // 6-7 the K rows and warps 8-9 the V rows
-    static constexpr int kConvWarpsK = kNc == 128 ? 4 : 2;
-    // 128-position chunks release the K and V halves of a 16-bit stage
-    // separately (K after S, V after PV); 64-position chunks release the stage
-    // as one after PV (measured faster there)
-    static constexpr bool kKVSplit = kNc == 128;
     static constexpr int kKBytes = kNc * D * 2;         // one K (or V) chunk
     static constexpr int kStageBytes = 2 * kKBytes;
     static constexpr int kF8Bytes = 2 * kNc * D;        // one 8-bit K + V chunk
@@ -85,18 +76,15 @@ template <int D, bool F8 = false> struct Cfg {
     static constexpr int kF8Off = kStageOff + kStages * kStageBytes;
     static constexpr int kBarOff = kF8Off + kF8Stages * kF8Bytes;
     static constexpr int kSmemBytes = kBarOff + 512 + 1024;   // + barriers + alignment slack
-    // Tensor memory (32-bit columns x 128 lanes; lane = query row of the tile):
-    // S double buffer, O accumulator, Q and P as 16-bit pairs (the A operands of
-    // the two MMAs).  64-position chunks: P has its own double buffer;
-    // 128-position chunks: P is written over the first half of its chunk's S
-    // buffer (the four would not fit in 512 columns).
-    static constexpr bool kAliasP = kNc == 128;
+    // Tensor memory (32-bit columns x 128 lanes): S double buffer, O
+    // accumulator, Q and the P double buffer as 16-bit pairs (the A operands of
+    // the two MMAs).
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kSCol = 0;                // 2 x kNc
     static constexpr uint32_t kOCol = 2 * kNc;          // D (<= 128)
     static constexpr uint32_t kQCol = kOCol + 128;      // D / 2
-    static constexpr uint32_t kPCol = kAliasP ? kSCol : kQCol + 64;
-    static constexpr uint32_t kPStride = kAliasP ? kNc : kNc / 2;   // columns between P buffers
+    static constexpr uint32_t kPCol = kQCol + 64;       // 2 x kNc / 2
+    static constexpr uint32_t kPStride = kNc / 2;       // columns between P buffers
 };
 
 struct TcArgs {
@@ -127,14 +115,11 @@ struct TcArgs {
 };
 
 struct Barriers {
-    uint64_t kv_full[8];      // FP8: the K half of the stage
+    uint64_t kv_full[8];
     uint64_t kv_empty[8];
-    uint64_t v_full[8];       // FP8 only: the V half of the stage
-    uint64_t v_empty[8];
     uint64_t s_full[2];
     uint64_t s_free[2];
     uint64_t p_full[2];
-    uint64_t pv_done;
     uint64_t p_free[2];
     uint64_t o_final;
     uint64_t q_full;
@@ -347,12 +332,9 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
 
     if (tid == 0) {
         for (int i = 0; i < C::kStages; ++i) {
-            // FP8: the converter warps that write K (all four for 128-position
-            // chunks, 6-7 for 64-position chunks) and those that write V
-            mbar_init(&bar.kv_full[i], F8 ? (C::kKVSplit ? C::kConvWarpsK : 4) : 1);
-            mbar_init(&bar.kv_empty[i], F8 ? 1 : 2);       // bf16: K read by S, V read by PV
-            mbar_init(&bar.v_full[i], C::kConvWarpsK);
-            mbar_init(&bar.v_empty[i], 1);
+            // FP8: the four converter warps (two write K, two V)
+            mbar_init(&bar.kv_full[i], F8 ? 4 : 1);
+            mbar_init(&bar.kv_empty[i], 1);                // PV (after S) has read the stage
         }
         for (int i = 0; i < C::kF8Stages; ++i) {
             mbar_init(&bar.f8_full[i], 1);
@@ -363,7 +345,6 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             mbar_init(&bar.s_free[i], 4);
             mbar_init(&bar.p_full[i], 4);
         }
-        mbar_init(&bar.pv_done, 1);
         mbar_init(&bar.o_final, 1);
         mbar_init(&bar.q_full, 4);
         mbar_init(&bar.drain, F8 ? 1 : 2);
@@ -390,6 +371,20 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
     auto fail = [&]() {
         *abort = 1;
         rd_flag(a.status, RD_DEV_TIMEOUT);
+    };
+    // O += P V for chunk gp (K-steps of 16 positions; A = P in TMEM, B = the V
+    // stage); the commits release the stage (S of the chunk completed before
+    // its P was written) and the P buffer.
+    auto issue_pv = [&](uint32_t gp, bool first, uint64_t v_desc) {
+        constexpr uint32_t idPV = F8 ? idesc_f16(kM, D, false, true) : idesc_bf16(kM, D, false, true);
+        const uint64_t vd = v_desc + (uint64_t)(((gp % C::kStages) * C::kStageBytes) >> 4);
+        const uint32_t pt = tmem + C::kPCol + (gp & 1) * C::kPStride;
+#pragma unroll
+        for (int kk = 0; kk < C::kNc / 16; ++kk)
+            mma_tmem_a(tmem + C::kOCol, pt + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), idPV,
+                       !(first && kk == 0));
+        mma_commit(&bar.kv_empty[gp % C::kStages]);
+        mma_commit(&bar.p_free[gp & 1]);
     };
 
     if (F8 && warp == kProducerWarp) {
@@ -421,15 +416,11 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
         }
     } else if (F8 && warp >= kConvWarp0) {
         // ------------------------------------------------------------ converters
-        // K and V halves of a 16-bit stage are filled and released separately: K
-        // as soon as S has read it, V once PV has.  128-position chunks: thread
-        // ct converts row ct of K and of V; 64-position chunks: threads 0-63
-        // convert the K rows, threads 64-127 the V rows.
+        // Threads 0-63 write the K rows of a 16-bit stage, threads 64-127 its V
+        // rows; the stage is released as one once PV has read it.
         const int ct = tid - kConvWarp0 * 32;
-        constexpr bool kHalves = C::kNc == 64;
-        const int row = kHalves ? (ct & 63) : ct;
-        const bool do_k = !kHalves || ct < 64;     // warp-uniform
-        const bool do_v = !kHalves || ct >= 64;
+        const int row = ct & 63;
+        const bool do_k = ct < 64;                 // warp-uniform
         uint32_t g = 0, g8 = 0;
         // one 128-byte e4m3 row (swizzled) -> one 256-byte f16 row in two 128-byte blocks
         auto widen_row = [&](const unsigned char* src, unsigned char* dst) {
@@ -481,46 +472,21 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                     ok = false;
                     break;
                 }
-                if (!C::kKVSplit && g >= (uint32_t)C::kStages &&
-                    !warp_wait(&bar.kv_empty[st], prev, abort, kWaitBudget)) {
+                if (g >= (uint32_t)C::kStages && !warp_wait(&bar.kv_empty[st], prev, abort, kWaitBudget)) {
                     ok = false;
                     break;
                 }
-                // ---- K half ----
+                const int d = (j - geo.n_ctx) * C::kNc + row;       // draft row (drafts only)
                 if (do_k) {
-                    if (C::kKVSplit && g >= (uint32_t)C::kStages &&
-                        !warp_wait(&bar.kv_empty[st], prev, abort, kWaitBudget)) {
-                        ok = false;
-                        break;
-                    }
                     if (ctx) widen_row(src, kdst);
-                    else draft_row(a.k_new, geo, (j - geo.n_ctx) * C::kNc + row, a.k_inv, kdst);
-                    if (C::kKVSplit) {
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&bar.kv_full[st]);
-                    }
-                }
-                // ---- V half ----
-                if (do_v) {
-                    if (C::kKVSplit && g >= (uint32_t)C::kStages &&
-                        !warp_wait(&bar.v_empty[st], prev, abort, kWaitBudget)) {
-                        ok = false;
-                        break;
-                    }
+                    else draft_row(a.k_new, geo, d, a.k_inv, kdst);
+                } else {
                     if (ctx) widen_row(src + C::kNc * D, vdst);
-                    else draft_row(a.v_new, geo, (j - geo.n_ctx) * C::kNc + row, a.v_inv, vdst);
-                    if (C::kKVSplit) {
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&bar.v_full[st]);
-                    }
+                    else draft_row(a.v_new, geo, d, a.v_inv, vdst);
                 }
-                if (!C::kKVSplit) {                 // the whole stage at once
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bar.kv_full[st]);
-                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar.kv_full[st]);
                 if (ctx && lane == 0) mbar_arrive(&bar.f8_empty[s8]);
                 if (ctx) ++g8;
             }
@@ -580,42 +546,20 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 mbar_wait(&bar.kv_full[k % C::kStages], (k / C::kStages) & 1, &no_abort, kWaitBudget);
         }
     } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------ MMA issuer
-        // bf16: S = Q K^T only (the PV issuer runs in its own warp, so the two
-        // chains overlap); FP8: S and O += P V from this one thread.
+        // ------------------------------------------------------- S issuer
+        // S = Q K^T for every chunk as soon as it has landed and its TMEM tile is
+        // free.  bf16: PV runs from its own warp, so the two chains overlap.
+        // FP8: this thread also issues PV_{j-1} right after S_j, once the
+        // softmax has written P_{j-1} (measured faster there than a PV warp).
         if (lane == 0) {
             constexpr uint32_t idS = F8 ? idesc_f16(kM, C::kNc, false, false) : idesc_bf16(kM, C::kNc, false, false);
-            constexpr uint32_t idPV = F8 ? idesc_f16(kM, D, false, true) : idesc_bf16(kM, D, false, true);
             uint32_t g = 0, unit_iter = 0;
             // Shared-memory descriptors differ only in their start-address field
-            // (bits 0-13, address >> 4): build each base once and add offsets,
+            // (bits 0-13, address >> 4): build the base once and add offsets,
             // which keeps the issuing thread's work per MMA to two additions.
             const uint64_t k_desc = smem_desc(smem_addr(smem + C::kStageOff), 16, 1024, kSwizzle128B);
             const uint64_t v_desc = smem_desc(smem_addr(smem + C::kStageOff + C::kKBytes), C::kNc * 128,
                                               1024, kSwizzle128B);
-            // S = Q K^T for chunk gs (D/16 K-steps) into TMEM tile gs & 1.
-            auto issue_s = [&](uint32_t gs) {
-                const uint64_t kd = k_desc + (uint64_t)(((gs % C::kStages) * C::kStageBytes) >> 4);
-                const uint32_t d_tmem = tmem + C::kSCol + (gs & 1) * C::kNc;
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = ((ks >> 2) * (C::kNc * 128) + (ks & 3) * 32) >> 4;
-                    mma_tmem_a(d_tmem, tmem + C::kQCol + ks * 8, kd + off, idS, ks > 0);
-                }
-                mma_commit(&bar.s_full[gs & 1]);
-            };
-            // O += P V for chunk gp (K-steps of 16 positions).
-            auto issue_pv = [&](uint32_t gp, bool first) {
-                const uint64_t vd = v_desc + (uint64_t)(((gp % C::kStages) * C::kStageBytes) >> 4);
-                const uint32_t pt = tmem + C::kPCol + (gp & 1) * C::kPStride;
-#pragma unroll
-                for (int kk = 0; kk < C::kNc / 16; ++kk)
-                    mma_tmem_a(tmem + C::kOCol, pt + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), idPV,
-                               !(first && kk == 0));
-                mma_commit(C::kKVSplit ? &bar.v_empty[gp % C::kStages] : &bar.kv_empty[gp % C::kStages]);
-                mma_commit(&bar.p_free[gp & 1]);
-                mma_commit(&bar.pv_done);
-            };
             for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
                 const UnitGeo geo = unit_geo<C::kNc>(a, u);
                 if (!geo.live) continue;
@@ -623,50 +567,43 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 if (!mbar_wait(&bar.q_full, unit_iter & 1, abort, kWaitBudget)) { fail(); break; }
                 tc_fence_after();
                 bool ok = true;
-                // S_j as soon as chunk j has landed and its TMEM tile is free; FP8:
-                // then PV_{j-1} once the softmax has written P_{j-1}.
-                for (int j = 0; j < n && ok; ++j) {
+                for (int j = 0; j < n; ++j) {
                     const uint32_t gg = g + j;
-                    // 128-position chunks: P_{j-2} lives in the S buffer that S_j
-                    // overwrites, so S_j also waits for PV_{j-2} to complete
                     if (!mbar_wait(&bar.kv_full[gg % C::kStages], (gg / C::kStages) & 1, abort, kWaitBudget) ||
-                        (gg >= 2 && !mbar_wait(&bar.s_free[gg & 1], ((gg >> 1) - 1) & 1, abort, kWaitBudget)) ||
-                        (C::kAliasP && gg >= 2 &&
-                         !mbar_wait(&bar.p_free[gg & 1], ((gg >> 1) - 1) & 1, abort, kWaitBudget))) {
+                        (gg >= 2 && !mbar_wait(&bar.s_free[gg & 1], ((gg >> 1) - 1) & 1, abort, kWaitBudget))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    issue_s(gg);
-                    if (!F8 || C::kKVSplit)
-                        mma_commit(&bar.kv_empty[gg % C::kStages]);     // K of the stage read
+                    // D/16 K-steps into TMEM tile gg & 1
+                    const uint64_t kd = k_desc + (uint64_t)(((gg % C::kStages) * C::kStageBytes) >> 4);
+                    const uint32_t d_tmem = tmem + C::kSCol + (gg & 1) * C::kNc;
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint32_t off = ((ks >> 2) * (C::kNc * 128) + (ks & 3) * 32) >> 4;
+                        mma_tmem_a(d_tmem, tmem + C::kQCol + ks * 8, kd + off, idS, ks > 0);
+                    }
+                    mma_commit(&bar.s_full[gg & 1]);
                     if (F8 && j >= 1) {
-                        const uint32_t gp = gg - 1;
-                        if (!mbar_wait(&bar.p_full[gp & 1], (gp >> 1) & 1, abort, kWaitBudget) ||
-                            (C::kKVSplit && !mbar_wait(&bar.v_full[gp % C::kStages], (gp / C::kStages) & 1,
-                                                       abort, kWaitBudget))) {
+                        if (!mbar_wait(&bar.p_full[(gg - 1) & 1], ((gg - 1) >> 1) & 1, abort, kWaitBudget)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        issue_pv(gg - 1, j == 1);
+                        issue_pv(gg - 1, j == 1, v_desc);
                     }
                 }
-                if constexpr (F8) {
-                    if (ok) {
-                        const uint32_t gl = g + n - 1;
-                        if (!mbar_wait(&bar.p_full[gl & 1], (gl >> 1) & 1, abort, kWaitBudget) ||
-                            (C::kKVSplit && !mbar_wait(&bar.v_full[gl % C::kStages], (gl / C::kStages) & 1,
-                                                       abort, kWaitBudget)))
-                            ok = false;
-                        else {
-                            tc_fence_after();
-                            issue_pv(gl, n == 1);
-                        }
+                if (F8 && ok) {
+                    const uint32_t gl = g + n - 1;
+                    if (!mbar_wait(&bar.p_full[gl & 1], (gl >> 1) & 1, abort, kWaitBudget)) {
+                        ok = false;
+                    } else {
+                        tc_fence_after();
+                        issue_pv(gl, n == 1, v_desc);
                     }
                 }
                 if (!ok) { fail(); break; }
-                if constexpr (F8) mma_commit(&bar.o_final);
+                if (F8) mma_commit(&bar.o_final);
                 g += n;
                 ++unit_iter;
             }
@@ -676,11 +613,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
         }
     } else if (!F8 && warp == kPvWarp) {
         // ------------------------------------------------------- PV issuer (bf16)
-        // O += P V for every chunk once the softmax has written its P; the P
-        // buffer is released per buffer (p_free) and the stage's V read is the
-        // second arrival on kv_empty.
         if (lane == 0) {
-            constexpr uint32_t idPV = idesc_bf16(kM, D, false, true);
             uint32_t g = 0;
             const uint64_t v_desc = smem_desc(smem_addr(smem + C::kStageOff + C::kKBytes), C::kNc * 128,
                                               1024, kSwizzle128B);
@@ -696,14 +629,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t vd = v_desc + (uint64_t)(((gg % C::kStages) * C::kStageBytes) >> 4);
-                    const uint32_t pt = tmem + C::kPCol + (gg & 1) * C::kPStride;
-#pragma unroll
-                    for (int kk = 0; kk < C::kNc / 16; ++kk)
-                        mma_tmem_a(tmem + C::kOCol, pt + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), idPV,
-                                   !(j == 0 && kk == 0));
-                    mma_commit(&bar.kv_empty[gg % C::kStages]);
-                    mma_commit(&bar.p_free[gg & 1]);
+                    issue_pv(gg, j == 0, v_desc);
                 }
                 if (!ok) { fail(); break; }
                 mma_commit(&bar.o_final);
@@ -714,14 +640,23 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
         }
     } else {
         // ------------------------------------------------------------ softmax
-        const int t = tid;                                 // row within the tile = TMEM lane
+        // Thread tid owns TMEM lane tid.  A tile with more than 64 valid rows
+        // keeps row r in lane r, and a thread takes all 64 columns of a chunk.
+        // A tile with at most 64 valid rows is paired: row r = 16 w + (lane & 15)
+        // of warp w sits in lanes lane and lane ^ 16 of that warp (both hold its
+        // query, hence the same scores), and each lane takes 32 of the chunk's
+        // columns.  A lane's P row is zero outside its own columns, so its O is
+        // the partial sum over them; the two lanes share one running maximum
+        // (exchanged every chunk), so their rescales agree and their O and l add
+        // up in the epilogue.  All four warps then share the exponentials of up
+        // to 64 rows instead of two warps taking every column.
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         uint32_t g = 0, unit_iter = 0;
         for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
             const UnitGeo geo = unit_geo<C::kNc>(a, u);
-            const int row = geo.tile * kM + t;
             const int hq0 = geo.h * a.G;
             if (geo.zero_tile) {                           // padded rows of a tree tile
+                const int row = geo.tile * kM + tid;
                 const int p = row / a.G;
                 if (p < a.P_max) {
                     uint4* dst = reinterpret_cast<uint4*>(
@@ -733,6 +668,10 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             }
             if (!geo.live) continue;
             const int n = geo.n_ctx + geo.n_draft;
+            const bool paired = geo.n_rows - geo.tile * kM <= 64;   // the same for the whole CTA
+            const int hf = paired ? lane >> 4 : 0;         // column half of a paired lane
+            const int r = paired ? warp * 16 + (lane & 15) : tid;   // row within the tile
+            const int row = geo.tile * kM + r;
             const bool valid = row < geo.n_rows;
             const int qpos = row / a.G;                    // node p (tree) / token t (causal)
             // ---- queries -> tensor memory (this thread's lane, 16-bit pairs) -----
@@ -764,112 +703,75 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 if (lane == 0) mbar_arrive(&bar.q_full);
             }
             float m = -INFINITY, l = 0.f;
-            // a warp whose 32 rows are all padding reads no scores: it keeps the
+            // a warp whose rows are all padding reads no scores: it keeps the
             // barrier protocol and zeroes its P rows once per buffer and unit
             const bool dead = __all_sync(0xffffffffu, !valid);
             const uint32_t* mrow = (!a.causal && valid)
                 ? a.mask + ((size_t)geo.b * a.P_max + qpos) * a.mask_words : nullptr;
-            bool ok = true;
-            for (int j = 0; j < n; ++j) {
-                const uint32_t gg = g + j;
+            // One chunk: NCOL = 64 columns per lane, or 32 for a paired lane.
+            auto chunk = [&](auto ncol, uint32_t gg, int j) -> bool {
+                constexpr int NCOL = decltype(ncol)::value;
                 const int sb = gg & 1;
-                if (!warp_wait(&bar.s_full[sb], (gg >> 1) & 1, abort, kWaitBudget)) { ok = false; break; }
-                tc_fence_after();
-                constexpr int kH = C::kNc / 64;            // 64-column parts of a chunk
+                const int c0 = NCOL == 32 ? 32 * hf : 0;  // first column of this lane
                 const uint32_t p_col = tmem + lane_base + C::kPCol + sb * C::kPStride;
-                if (dead) {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bar.s_free[sb]);
-                    // bf16: like the live warps, arrive for chunk gg only once PV of
-                    // chunk gg-2 has released the buffer, so that no arrival runs
-                    // ahead into an earlier phase of p_full
-                    if (!F8 && gg >= 2 &&
-                        !warp_wait(&bar.p_free[sb], ((gg >> 1) - 1) & 1, abort, kWaitBudget)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    // zero P rows once per buffer and unit, or every chunk when P
-                    // shares its columns with S, which the MMA rewrites
-                    if (C::kAliasP || j < 2) {
-                        uint32_t zero[32];
-#pragma unroll
-                        for (int c = 0; c < 32; ++c) zero[c] = 0u;
-#pragma unroll
-                        for (int h = 0; h < kH; ++h) tmem_st32(p_col + h * 32, zero);
-                        tmem_st_wait();
-                    }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bar.p_full[sb]);
-                    continue;
-                }
-                // scores of part h (64 columns) from TMEM
-                auto load_part = [&](int h, float (&s)[64]) {
+                float s[NCOL];
+                {
+                    // the load is warp-collective (one address for all lanes): read
+                    // all 64 columns; a paired lane keeps its 32
                     uint32_t sr[64];
-                    const uint32_t s_col = tmem + lane_base + C::kSCol + sb * C::kNc + h * 64;
+                    const uint32_t s_col = tmem + lane_base + C::kSCol + sb * C::kNc;
                     tmem_ld32(s_col, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
                     tmem_ld32(s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
                     tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c]);
-                };
-                // ---- visibility of part h -------------------------------------------
-                auto mask_part = [&](int h, float (&s)[64]) {
-                    if (!valid) {
-#pragma unroll
-                        for (int c = 0; c < 64; ++c) s[c] = -INFINITY;
-                    } else if (j < geo.n_ctx) {
-                        const int pos0 = (geo.c_first + j) * C::kNc + h * 64;
-                        const int lim = a.causal ? min(geo.C, qpos + 1) : geo.C;   // visible: pos < lim
-                        if (pos0 + 64 > lim) {
-#pragma unroll
-                            for (int c = 0; c < 64; ++c)
-                                if (pos0 + c >= lim) s[c] = -INFINITY;
-                        }
-                    } else {
-                        const int d0 = (j - geo.n_ctx) * C::kNc + h * 64;
-                        const uint32_t w0 = (d0 >> 5) < a.mask_words ? __ldg(mrow + (d0 >> 5)) : 0u;
-                        const uint32_t w1 = (d0 >> 5) + 1 < a.mask_words ? __ldg(mrow + (d0 >> 5) + 1) : 0u;
-#pragma unroll
-                        for (int c = 0; c < 64; ++c) {
-                            const uint32_t w = c < 32 ? w0 : w1;
-                            const bool vis = (d0 + c < geo.Pb) && ((w >> (c & 31)) & 1u);
-                            if (!vis) s[c] = -INFINITY;
-                        }
-                    }
-                };
-                float s[64];
-                float mx = -INFINITY;
-#pragma unroll
-                for (int h = 0; h < kH; ++h) {
-                    load_part(h, s);
-                    if (kH == 1) {                         // S is in registers: release it
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&bar.s_free[sb]);
-                    }
-                    mask_part(h, s);
-                    // ---- online softmax (log2 domain) ----------------------------
-                    float mx8[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) mx8[e] = s[e];
-#pragma unroll
-                    for (int c = 8; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
-                    mx = fmaxf(mx, fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                         fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))));
+                    for (int c = 0; c < NCOL; ++c)
+                        s[c] = __uint_as_float(NCOL == 64 ? sr[c] : (hf ? sr[32 + c] : sr[c]));
                 }
+                tc_fence_before();                         // S is in registers: release it
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar.s_free[sb]);
+                // ---- visibility ---------------------------------------------------
+                if (!valid) {
+#pragma unroll
+                    for (int c = 0; c < NCOL; ++c) s[c] = -INFINITY;
+                } else if (j < geo.n_ctx) {
+                    const int pos0 = (geo.c_first + j) * C::kNc + c0;
+                    const int lim = a.causal ? min(geo.C, qpos + 1) : geo.C;   // visible: pos < lim
+                    if (pos0 + NCOL > lim) {
+#pragma unroll
+                        for (int c = 0; c < NCOL; ++c)
+                            if (pos0 + c >= lim) s[c] = -INFINITY;
+                    }
+                } else {
+                    const int d0 = (j - geo.n_ctx) * C::kNc + c0;          // a multiple of 32
+                    const uint32_t w0 = (d0 >> 5) < a.mask_words ? __ldg(mrow + (d0 >> 5)) : 0u;
+                    const uint32_t w1 = (NCOL == 64 && (d0 >> 5) + 1 < a.mask_words)
+                        ? __ldg(mrow + (d0 >> 5) + 1) : 0u;
+#pragma unroll
+                    for (int c = 0; c < NCOL; ++c) {
+                        const uint32_t w = c < 32 ? w0 : w1;
+                        const bool vis = (d0 + c < geo.Pb) && ((w >> (c & 31)) & 1u);
+                        if (!vis) s[c] = -INFINITY;
+                    }
+                }
+                // ---- online softmax (log2 domain) --------------------------------
+                float mx8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) mx8[e] = s[e];
+#pragma unroll
+                for (int c = 8; c < NCOL; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+                float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                if constexpr (NCOL == 32) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
                 const float ms = mx * a.scale_log2;
                 const bool need = ms > m + kRescaleThreshold;
                 const float m_new = need ? ms : m;
                 if (__any_sync(0xffffffffu, need) && j > 0) {
-                    // O holds earlier chunks: wait for PV of the previous chunk, then rescale
-                    // (bf16: PV_{j-1} is done when it has released its P buffer; a
-                    // per-buffer barrier cannot lag two phases behind the wait)
-                    const bool pv_prev = F8 ? warp_wait(&bar.pv_done, (gg - 1) & 1, abort, kWaitBudget)
-                                            : warp_wait(&bar.p_free[(gg - 1) & 1], ((gg - 1) >> 1) & 1,
-                                                        abort, kWaitBudget);
-                    if (!pv_prev) { ok = false; break; }
+                    // O holds earlier chunks: wait until PV of the previous chunk has
+                    // completed (it then releases its P buffer; a per-buffer barrier
+                    // cannot lag two phases behind the wait), then rescale
+                    if (!warp_wait(&bar.p_free[(gg - 1) & 1], ((gg - 1) >> 1) & 1, abort, kWaitBudget))
+                        return false;
                     tc_fence_after();
                     const float alpha = need ? fast_exp2(m - m_new) : 1.f;
 #pragma unroll
@@ -889,54 +791,93 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 }
                 const float base = (m == -INFINITY) ? 0.f : m;
                 float lsum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                uint32_t pv[NCOL / 2];
 #pragma unroll
-                for (int h = 0; h < kH; ++h) {
-                    if (kH > 1) {                          // FP8: read part h again
-                        load_part(h, s);
-                        mask_part(h, s);
+                for (int c8 = 0; c8 < NCOL / 8; ++c8) {
+                    float p[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        p[e] = fast_exp2(fmaf(s[c8 * 8 + e], a.scale_log2, -base));
+                        lsum[e] += p[e];
                     }
-                    uint32_t pv[32];
 #pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8) {
-                        float p[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            p[e] = fast_exp2(fmaf(s[c8 * 8 + e], a.scale_log2, -base));
-                            lsum[e] += p[e];
-                        }
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) pv[c8 * 4 + e] = pack16<F8>(p[2 * e], p[2 * e + 1]);
-                    }
-                    // P (16-bit) into this lane's P columns: PV's A operand (bf16: once
-                    // PV of the chunk two back has released that buffer; FP8: S_j was
-                    // issued after PV_{j-2}, and s_full(j) covers the completion of every
-                    // earlier MMA of that issuer; with P over S, part h overwrites only
-                    // S columns already read)
-                    if (h == 0) {
-                        if (!F8 && gg >= 2 &&
-                            !warp_wait(&bar.p_free[sb], ((gg >> 1) - 1) & 1, abort, kWaitBudget)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                    }
-                    tmem_st32(p_col + h * 32, pv);
+                    for (int e = 0; e < 4; ++e) pv[c8 * 4 + e] = pack16<F8>(p[2 * e], p[2 * e + 1]);
                 }
-                if (!ok) break;
+                // P (16-bit) into this lane's P columns, PV's A operand, once PV of
+                // the chunk two back has released that buffer; a paired lane
+                // writes zeros over the other lane's columns
+                if (gg >= 2 && !warp_wait(&bar.p_free[sb], ((gg >> 1) - 1) & 1, abort, kWaitBudget))
+                    return false;
+                tc_fence_after();
+                if constexpr (NCOL == 64) {
+                    tmem_st32(p_col, pv);
+                } else {
+                    uint32_t pw[32];
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) pw[c] = ((c >> 4) == hf) ? pv[c & 15] : 0u;
+                    tmem_st32(p_col, pw);
+                }
                 l += ((lsum[0] + lsum[1]) + (lsum[2] + lsum[3])) +
                      ((lsum[4] + lsum[5]) + (lsum[6] + lsum[7]));
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (kH > 1 && lane == 0) mbar_arrive(&bar.s_free[sb]);
                 if (lane == 0) mbar_arrive(&bar.p_full[sb]);
+                return true;
+            };
+            bool ok = true;
+            for (int j = 0; j < n; ++j) {
+                const uint32_t gg = g + j;
+                const int sb = gg & 1;
+                if (!warp_wait(&bar.s_full[sb], (gg >> 1) & 1, abort, kWaitBudget)) { ok = false; break; }
+                tc_fence_after();
+                if (dead) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar.s_free[sb]);
+                    // like the live warps, arrive for chunk gg only once PV of chunk
+                    // gg-2 has released the buffer, so that no arrival runs ahead
+                    // into an earlier phase of p_full
+                    if (gg >= 2 && !warp_wait(&bar.p_free[sb], ((gg >> 1) - 1) & 1, abort, kWaitBudget)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (j < 2) {                           // zero P rows once per buffer and unit
+                        uint32_t zero[32];
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) zero[c] = 0u;
+                        tmem_st32(tmem + lane_base + C::kPCol + sb * C::kPStride, zero);
+                        tmem_st_wait();
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar.p_full[sb]);
+                    continue;
+                }
+                ok = paired ? chunk(std::integral_constant<int, 32>{}, gg, j)
+                            : chunk(std::integral_constant<int, 64>{}, gg, j);
+                if (!ok) break;
             }
             if (!ok || !warp_wait(&bar.o_final, unit_iter & 1, abort, kWaitBudget)) { fail(); break; }
             tc_fence_after();
             // ---- epilogue ----------------------------------------------------------
+            // A paired row's O and l are the sums over its two lanes; lane half hf
+            // then writes output columns [hf D/2, (hf + 1) D/2).
+            const float l_row = paired ? l + __shfl_xor_sync(0xffffffffu, l, 16) : l;
+            auto o_block = [&](int cb, uint32_t (&o)[32]) {
+                tmem_ld32(tmem + lane_base + C::kOCol + cb * 32, o);
+                tmem_ld_wait();
+                if (paired) {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        o[c] = __float_as_uint(__uint_as_float(o[c]) +
+                                               __shfl_xor_sync(0xffffffffu, __uint_as_float(o[c]), 16));
+                }
+            };
+            auto mine = [&](int cb) { return !paired || (cb >= D / 64) == (hf == 1); };
             const bool split_mode = !a.causal && geo.n_splits > 1;
             if (!split_mode) {
-                const float inv = (valid && l > 0.f) ? a.out_scale / l : 0.f;
+                const float inv = (valid && l_row > 0.f) ? a.out_scale / l_row : 0.f;
                 const bool write = valid || (!a.causal && qpos < a.P_max);
                 uint16_t* dst = nullptr;
                 if (write) {
@@ -947,9 +888,8 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
 #pragma unroll
                 for (int cb = 0; cb < D / 32; ++cb) {
                     uint32_t o[32];
-                    tmem_ld32(tmem + lane_base + C::kOCol + cb * 32, o);
-                    tmem_ld_wait();
-                    if (write) {
+                    o_block(cb, o);
+                    if (write && mine(cb)) {
 #pragma unroll
                         for (int c = 0; c < 32; c += 8) {
                             uint4 v;
@@ -961,37 +901,54 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                         }
                     }
                 }
+                // paired: rows 64-127 of the tile hold no valid row; their padded
+                // outputs are zero (half a row per lane)
+                if (paired && !a.causal) {
+                    const int row2 = geo.tile * kM + 64 + r;
+                    if (row2 / a.G < a.P_max) {
+                        uint4* dst2 = reinterpret_cast<uint4*>(
+                            a.o + (((size_t)geo.b * a.P_max + row2 / a.G) * a.Hq + hq0 + row2 % a.G) * D +
+                            hf * (D / 2));
+#pragma unroll
+                        for (int c = 0; c < D / 16; ++c) dst2[c] = make_uint4(0, 0, 0, 0);
+                    }
+                }
             } else {
                 // fp32 partials; the CTA that takes the last ticket of (b, h, tile) merges
                 const size_t unit_id = ((size_t)geo.b * a.Hkv + geo.h) * a.tiles + geo.tile;
-                const size_t prow = unit_id * kM + t;
+                const size_t prow = unit_id * kM + r;
                 float* op = a.o_part + (prow * a.splits + geo.split) * D;
 #pragma unroll
                 for (int cb = 0; cb < D / 32; ++cb) {
                     uint32_t o[32];
-                    tmem_ld32(tmem + lane_base + C::kOCol + cb * 32, o);
-                    tmem_ld_wait();
+                    o_block(cb, o);
+                    if (mine(cb)) {
 #pragma unroll
-                    for (int c = 0; c < 32; c += 4)
-                        *reinterpret_cast<float4*>(op + cb * 32 + c) =
-                            make_float4(__uint_as_float(o[c]), __uint_as_float(o[c + 1]),
-                                        __uint_as_float(o[c + 2]), __uint_as_float(o[c + 3]));
+                        for (int c = 0; c < 32; c += 4)
+                            *reinterpret_cast<float4*>(op + cb * 32 + c) =
+                                make_float4(__uint_as_float(o[c]), __uint_as_float(o[c + 1]),
+                                            __uint_as_float(o[c + 2]), __uint_as_float(o[c + 3]));
+                    }
                 }
-                a.ml_part[prow * a.splits + geo.split] = make_float2(m, l);
+                if (hf == 0) a.ml_part[prow * a.splits + geo.split] = make_float2(m, l_row);
                 __threadfence();
                 asm volatile("bar.sync 1, %0;" ::"r"(kSoftmaxThreads));
-                if (t == 0) {
+                if (tid == 0) {
                     const unsigned tk = atomicAdd(a.tickets + unit_id, 1u);
                     s_last = (tk == (unsigned)geo.n_splits - 1u);
                 }
                 asm volatile("bar.sync 1, %0;" ::"r"(kSoftmaxThreads));
                 if (s_last) {
                     __threadfence();
-                    const int p = row / a.G;
+                    // paired: lane half 1 writes the zero rows 64-127 of the tile
+                    const int rr = hf == 0 ? r : 64 + r;
+                    const int row_m = geo.tile * kM + rr;
+                    const bool valid_m = hf == 0 && valid;
+                    const int p = row_m / a.G;
                     if (p < a.P_max)
-                        merge_split_row<D>(a, prow, geo.n_splits, valid,
-                                           a.o + (((size_t)geo.b * a.P_max + p) * a.Hq + hq0 + row % a.G) * D);
-                    if (t == 0) a.tickets[unit_id] = 0u;
+                        merge_split_row<D>(a, unit_id * kM + rr, valid_m ? geo.n_splits : 0, valid_m,
+                                           a.o + (((size_t)geo.b * a.P_max + p) * a.Hq + hq0 + row_m % a.G) * D);
+                    if (tid == 0) a.tickets[unit_id] = 0u;
                 }
             }
             g += n;
@@ -1149,17 +1106,6 @@ cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, in
         a.v_inv = 1.f / fp8->v_scale;
         a.out_scale = fp8->v_scale;
         a.scale_log2 *= fp8->k_scale;
-    }
-    if (fp8 != nullptr) {
-        // 128-position chunks: the same split lengths rounded up to whole chunks,
-        // so the splits (and the partials) never exceed the plan's; the workspace
-        // keeps the plan's layout below
-        constexpr int nc = Cfg<128, true>::kNc;
-        const long cc = ((long)max_kv + nc - 1) / nc;
-        const long cps = std::max<long>(1, ((long)plan.split_len + nc - 1) / nc);
-        a.chunks_per_split = (int)cps;
-        a.splits = (int)std::max<long>(1, (cc + cps - 1) / cps);
-        a.n_units = B * Hkv * plan.tiles * a.splits;
     }
     if (plan.splits > 1) {
         const size_t unit_rows = (size_t)B * Hkv * plan.tiles * kM;
