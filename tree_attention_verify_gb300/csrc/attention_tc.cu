@@ -77,14 +77,16 @@ template <int D, bool F8 = false> struct Cfg {
     static constexpr int kBarOff = kF8Off + kF8Stages * kF8Bytes;
     static constexpr int kSmemBytes = kBarOff + 512 + 1024;   // + barriers + alignment slack
     // Tensor memory (32-bit columns x 128 lanes): S double buffer, O
-    // accumulator, Q and the P double buffer as 16-bit pairs (the A operands of
-    // the two MMAs).
+    // accumulator, and as 16-bit pairs (the A operands of the two MMAs) the P
+    // double buffer and two Q buffers, one per unit parity, so that the next
+    // unit's queries can be written while the current unit drains.
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kSCol = 0;                // 2 x kNc
     static constexpr uint32_t kOCol = 2 * kNc;          // D (<= 128)
-    static constexpr uint32_t kQCol = kOCol + 128;      // D / 2
+    static constexpr uint32_t kQCol = kOCol + 128;      // D / 2, unit parity 0
     static constexpr uint32_t kPCol = kQCol + 64;       // 2 x kNc / 2
     static constexpr uint32_t kPStride = kNc / 2;       // columns between P buffers
+    static constexpr uint32_t kQStride = 128;           // Q of unit parity 1 at kQCol + 128
 };
 
 struct TcArgs {
@@ -581,7 +583,8 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks) {
                         const uint32_t off = ((ks >> 2) * (C::kNc * 128) + (ks & 3) * 32) >> 4;
-                        mma_tmem_a(d_tmem, tmem + C::kQCol + ks * 8, kd + off, idS, ks > 0);
+                        mma_tmem_a(d_tmem, tmem + C::kQCol + (unit_iter & 1) * C::kQStride + ks * 8,
+                                   kd + off, idS, ks > 0);
                     }
                     mma_commit(&bar.s_full[gg & 1]);
                     if (F8 && j >= 1) {
@@ -651,9 +654,44 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
         // up in the epilogue.  All four warps then share the exponentials of up
         // to 64 rows instead of two warps taking every column.
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        auto is_paired = [&](const UnitGeo& ug) { return ug.n_rows - ug.tile * kM <= 64; };
+        // the queries of unit ug -> Q buffer qb (this thread's lane, 16-bit pairs)
+        auto load_q = [&](const UnitGeo& ug, uint32_t qb) {
+            const bool pr = is_paired(ug);
+            const int qr = ug.tile * kM + (pr ? warp * 16 + (lane & 15) : tid);
+            const bool qv_ok = qr < ug.n_rows;
+            const uint4* src = nullptr;
+            if (qv_ok) {
+                const int qp = qr / a.G;
+                const size_t qrow = a.causal ? (size_t)(ug.kv_base + qp) : (size_t)ug.b * a.P_max + qp;
+                src = reinterpret_cast<const uint4*>(a.q + (qrow * a.Hq + ug.h * a.G + qr % a.G) * D);
+            }
+#pragma unroll
+            for (int half = 0; half < D / 64; ++half) {
+                uint32_t qv[32];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 v = qv_ok ? __ldg(src + half * 8 + c) : make_uint4(0, 0, 0, 0);
+                    if constexpr (F8) {
+                        v.x = bf16x2_to_f16x2(v.x, 1.f); v.y = bf16x2_to_f16x2(v.y, 1.f);
+                        v.z = bf16x2_to_f16x2(v.z, 1.f); v.w = bf16x2_to_f16x2(v.w, 1.f);
+                    }
+                    qv[c * 4 + 0] = v.x; qv[c * 4 + 1] = v.y;
+                    qv[c * 4 + 2] = v.z; qv[c * 4 + 3] = v.w;
+                }
+                tmem_st32(tmem + lane_base + C::kQCol + qb * C::kQStride + half * 32, qv);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.q_full);
+        };
         uint32_t g = 0, unit_iter = 0;
+        int q_unit = -1;                                   // unit whose queries are already written
+        int next_u = -1;                                   // unit whose geometry is in next_geo
+        UnitGeo next_geo;
         for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
-            const UnitGeo geo = unit_geo<C::kNc>(a, u);
+            const UnitGeo geo = next_u == u ? next_geo : unit_geo<C::kNc>(a, u);
             const int hq0 = geo.h * a.G;
             if (geo.zero_tile) {                           // padded rows of a tree tile
                 const int row = geo.tile * kM + tid;
@@ -668,40 +706,13 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             }
             if (!geo.live) continue;
             const int n = geo.n_ctx + geo.n_draft;
-            const bool paired = geo.n_rows - geo.tile * kM <= 64;   // the same for the whole CTA
+            const bool paired = is_paired(geo);
             const int hf = paired ? lane >> 4 : 0;         // column half of a paired lane
             const int r = paired ? warp * 16 + (lane & 15) : tid;   // row within the tile
             const int row = geo.tile * kM + r;
             const bool valid = row < geo.n_rows;
             const int qpos = row / a.G;                    // node p (tree) / token t (causal)
-            // ---- queries -> tensor memory (this thread's lane, 16-bit pairs) -----
-            {
-                const uint4* src = nullptr;
-                if (valid) {
-                    const size_t qrow = a.causal ? (size_t)(geo.kv_base + qpos)
-                                                 : (size_t)geo.b * a.P_max + qpos;
-                    src = reinterpret_cast<const uint4*>(a.q + (qrow * a.Hq + hq0 + row % a.G) * D);
-                }
-#pragma unroll
-                for (int half = 0; half < D / 64; ++half) {
-                    uint32_t qv[32];
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        uint4 v = valid ? __ldg(src + half * 8 + c) : make_uint4(0, 0, 0, 0);
-                        if constexpr (F8) {
-                            v.x = bf16x2_to_f16x2(v.x, 1.f); v.y = bf16x2_to_f16x2(v.y, 1.f);
-                            v.z = bf16x2_to_f16x2(v.z, 1.f); v.w = bf16x2_to_f16x2(v.w, 1.f);
-                        }
-                        qv[c * 4 + 0] = v.x; qv[c * 4 + 1] = v.y;
-                        qv[c * 4 + 2] = v.z; qv[c * 4 + 3] = v.w;
-                    }
-                    tmem_st32(tmem + lane_base + C::kQCol + half * 32, qv);
-                }
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar.q_full);
-            }
+            if (q_unit != u) load_q(geo, unit_iter & 1);   // not written ahead
             float m = -INFINITY, l = 0.f;
             // a warp whose rows are all padding reads no scores: it keeps the
             // barrier protocol and zeroes its P rows once per buffer and unit
@@ -857,6 +868,18 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 ok = paired ? chunk(std::integral_constant<int, 32>{}, gg, j)
                             : chunk(std::integral_constant<int, 64>{}, gg, j);
                 if (!ok) break;
+            }
+            // the next unit's queries (if it is live) into the other Q buffer, so
+            // that its first S MMA overlaps this unit's PV drain and epilogue (the
+            // buffer's previous reader, S of the unit before this one, has
+            // completed); its geometry is kept for the next iteration
+            if (ok && u + (int)gridDim.x < a.n_units) {
+                next_u = u + gridDim.x;
+                next_geo = unit_geo<C::kNc>(a, next_u);
+                if (next_geo.live) {
+                    load_q(next_geo, (unit_iter + 1) & 1);
+                    q_unit = next_u;
+                }
             }
             if (!ok || !warp_wait(&bar.o_final, unit_iter & 1, abort, kWaitBudget)) { fail(); break; }
             tc_fence_after();
