@@ -150,12 +150,16 @@ template <int NC>
 __device__ __forceinline__ UnitGeo unit_geo(const TcArgs& a, int u)
 {
     UnitGeo g;
-    const int per_bh = a.tiles * a.splits;
-    g.b = u / (a.Hkv * per_bh);
-    const int rem = u % (a.Hkv * per_bh);
-    g.h = rem / per_bh;
-    g.tile = (rem % per_bh) / a.splits;
-    g.split = rem % a.splits;
+    // Units run split-major, then tile, request and kv head: the CTAs take units
+    // round-robin, and this order spreads the dead units (splits past a short
+    // context, tiles past the valid rows) and the long and short causal tiles
+    // evenly over them.
+    const int bh = a.B * a.Hkv;
+    g.split = u / (a.tiles * bh);
+    const int rem = u % (a.tiles * bh);
+    g.tile = rem / bh;
+    g.b = (rem % bh) / a.Hkv;
+    g.h = rem % a.Hkv;
     g.live = false;
     g.zero_tile = false;
     g.n_draft = 0;
