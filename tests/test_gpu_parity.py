@@ -421,3 +421,44 @@ def test_tree_attention_maximum_packed_length():
     pk = oracle.oracle_pack(inp["beams"].numpy(), cfg.P_max)
     assert pk["packed_len"].max() > 192              # the last draft chunk is used
     _attention_case(inp)
+
+
+def test_tree_attention_reused_workspace_split_launches():
+    # every split-KV launch must leave the workspace's merge tickets at zero,
+    # so the same workspace gives the same results call after call
+    rd = _rd()
+    cfg = workloads.CONFIGS["8b_gqa_b16"]
+    inp = workloads.make_verify_inputs(cfg, device=DEV)
+    st = _status()
+    pk = rd.rd_pack_beams(inp["beams"], cfg.P_max, dev_status=st)
+    max_ctx = int(inp["ctx_lens"].max())
+    n_ws = rd.rd_tree_attention_workspace_size(cfg.B, cfg.P_max, cfg.Hq, cfg.Hkv, cfg.D, max_ctx)
+    assert n_ws > 0                                      # this workload splits
+    ws = torch.zeros(n_ws, dtype=torch.uint8, device=DEV)
+    G = cfg.Hq // cfg.Hkv
+    tiles = -(-cfg.P_max * G // 128)
+    n_tail = cfg.B * cfg.Hkv * tiles * 4                 # the merge tickets end the workspace
+    outs = []
+    for _ in range(3):
+        o = rd.rd_tree_attention(inp["q"], inp["k_draft"], inp["v_draft"], inp["k_cache"],
+                                 inp["v_cache"], inp["ctx_offsets"], pk["packed_len"], pk["mask"],
+                                 max_ctx=max_ctx, workspace=ws, dev_status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        assert int(ws[-n_tail:].count_nonzero()) == 0
+        outs.append(o.clone())
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    rng = np.random.default_rng(5)
+    sample = [(int(rng.integers(cfg.B)), int(rng.integers(cfg.Hkv))) for _ in range(3)]
+    offs = inp["ctx_offsets"].cpu().numpy()
+    pk_ref = oracle.oracle_pack(inp["beams"].cpu().numpy(), cfg.P_max)
+    got = outs[2].float().cpu().numpy()
+    for b, h in sample:
+        sl = slice(int(offs[b]), int(offs[b + 1]))
+        hs = slice(h * G, (h + 1) * G)
+        ref = oracle.oracle_tree_attention(
+            bf16_bits(inp["q"][b:b + 1, :, hs]), bf16_bits(inp["k_draft"][b:b + 1, :, h:h + 1]),
+            bf16_bits(inp["v_draft"][b:b + 1, :, h:h + 1]), bf16_bits(inp["k_cache"][sl, h:h + 1]),
+            bf16_bits(inp["v_cache"][sl, h:h + 1]), np.array([0, offs[b + 1] - offs[b]], np.int64),
+            pk_ref["packed_len"][b:b + 1], pk_ref["mask"][b:b + 1])
+        _close(got[b:b + 1, :, hs], ref, f"{cfg.name} b={b} h={h}")

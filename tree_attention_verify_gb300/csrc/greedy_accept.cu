@@ -22,7 +22,7 @@
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kVecPerIter = 8;          // 16-byte loads in flight per thread
+constexpr int kVecPerIter = 4;          // 16-byte loads in flight per thread
 constexpr int kNoIndex = 0x7fffffff;
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p)

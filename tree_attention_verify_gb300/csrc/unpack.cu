@@ -24,21 +24,7 @@ unpack_kernel(const T* __restrict__ packed, int P_max, size_t row_words,
         return;
     }
     const T* src = packed + ((size_t)b * P_max + p) * row_words;
-    // up to kInFlight loads issued before the first store
-    constexpr int kInFlight = 8;
-    for (size_t k0 = threadIdx.x; k0 < row_words; k0 += (size_t)blockDim.x * kInFlight) {
-        T v[kInFlight];
-#pragma unroll
-        for (int i = 0; i < kInFlight; ++i) {
-            const size_t k = k0 + (size_t)i * blockDim.x;
-            if (k < row_words) v[i] = __ldg(src + k);
-        }
-#pragma unroll
-        for (int i = 0; i < kInFlight; ++i) {
-            const size_t k = k0 + (size_t)i * blockDim.x;
-            if (k < row_words) dst[k] = v[i];
-        }
-    }
+    for (size_t k = threadIdx.x; k < row_words; k += blockDim.x) dst[k] = __ldg(src + k);
 }
 
 }  // namespace
