@@ -1,40 +1,40 @@
-// Tree attention (generation phase) and causal prefill (context phase) on the
-// 5th-generation tensor cores: TMA-fed, tcgen05 MMA with TMEM accumulators,
-// warp-specialised, persistent.
+// Tree attention (generation phase) and causal prefill (context phase) on the 5th-
+// generation tensor cores: TMA-fed, tcgen05 MMA with TMEM accumulators, persistent.
 //
-// A single kernel with a topology-aware mask verifies every candidate path at
-// once (speculative-decoding survey page, SpecInfer "Token Tree Verifier"), and
-// TensorRT-LLM's attention plugin splits context and generation requests
-// (NVIDIA blog "ReDrafter in TensorRT-LLM", section "Inflight-batching
-// Compatible Engine").
+// A single kernel with a topology-aware mask verifies every candidate path at once
+// (speculative-decoding survey page, SpecInfer "Token Tree Verifier"); TensorRT-LLM's
+// attention plugin splits context and generation requests (NVIDIA blog "ReDrafter
+// in TensorRT-LLM", section "Inflight-batching Compatible Engine").
 //
 // Work unit = (request b, kv head h, 128-row query tile, KV split).  The G query
 // heads that share kv head h are stacked as rows (row r -> node p = r / G, head
 // h*G + r % G; causal: token t = r / G), so each K/V byte is read once per tile.
-// Row r of a tile is TMEM lane r.  A unit walks its KV chunks (64 positions):
-// first the context (all visible; the last chunk is ragged), then
-// the packed drafts (visible iff the node's ancestor-mask bit is set).
+// A unit walks its KV chunks (64 positions): the context (all visible, the last
+// chunk ragged), then the packed drafts (visible iff the node's ancestor-mask
+// bit is set).  CTAs take units round-robin in split-major order.
 //
 // Warp roles (one CTA per SM, persistent over units):
-//   warps 0-3  softmax: TMEM lane = row.  Write the tile's queries into TMEM,
-//              turn S into 16-bit probabilities P in TMEM (online softmax in
-//              exp2 form, rescaling O in TMEM only when a row maximum grows by
-//              more than 2^8), and write the output rows.
+//   warps 0-3  softmax: row r is TMEM lane r (a tile of <= 64 valid rows puts a
+//              row in two lanes, each taking half of a chunk's columns).  Write
+//              queries into TMEM (the next unit's into a second buffer before
+//              this unit's epilogue), turn S into 16-bit P in TMEM (online
+//              softmax in exp2 form, O rescaled only when a row maximum grows
+//              by more than 2^8), and write the output rows.
 //   warp 4     producer: TMA loads of K and V chunks (128-byte swizzle) into a
 //              ring of stages.
 //   warp 5     S issuer: S = Q K^T (M=128, N=chunk, K=D; A = Q in TMEM) into a
 //              double-buffered TMEM tile.
-//   warp 6     PV issuer: O += P V (M=128, N=D, K=chunk; A = P in TMEM) into
-//              TMEM.  The two issuers run independently.
+//   warp 6     PV issuer: O += P V (M=128, N=D, K=chunk; A = P in TMEM) into TMEM;
+//              the two issuers run independently.
 // FP8 variant (template flag F8; context K/V stored as e4m3 with per-tensor
-// scales): the producer TMA-loads e4m3 context chunks into an 8-bit ring;
-// warps 6-9 widen them (exactly) into the 16-bit ring the MMA reads, and
-// convert the bf16 draft chunks, divided by the scales, the same way; warp 5
-// issues both S and PV.  The MMA runs kind::f16 with f16 operands (e4m3 widens to f16 exactly and both
-// operands of one MMA share a type); the K scale is
-// folded into the softmax scale and the V scale into the output normalisation.
-// Every wait is bounded by a clock budget; on expiry the CTA records
-// RD_DEV_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM and exits.
+// scales): the producer TMA-loads e4m3 context chunks into an 8-bit ring; warps
+// 6-9 widen them (exactly) into the 16-bit ring the MMA reads, and convert the
+// bf16 draft chunks, divided by the scales, the same way; warp 5 issues S and PV.
+// The MMA runs kind::f16 with f16 operands (e4m3 widens to f16 exactly; both operands
+// of one MMA share a type); the K scale is folded into the softmax scale, the V scale
+// into the output normalisation.
+// Every wait is bounded by a clock budget; on expiry the CTA records RD_DEV_TIMEOUT,
+// drains its in-flight copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
