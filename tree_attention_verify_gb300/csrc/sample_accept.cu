@@ -260,6 +260,10 @@ sample_accept_kernel(const uint16_t* __restrict__ target, const uint16_t* __rest
         s_token[c] = tok;
     }
     __syncthreads();
+    // a peer stores into this CTA's shared memory only once every CTA of the
+    // cluster has started: arrive now, wait before the walk (whose cluster
+    // reductions do the remote stores); every CTA of the cluster gets here
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
     const float* ua = u_accept + (size_t)b * P_max;
     const float* us = u_sample + (size_t)b * V;
@@ -278,6 +282,7 @@ sample_accept_kernel(const uint16_t* __restrict__ target, const uint16_t* __rest
             }
         }
     }
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
     int slot = 0;
     int node = 0, a = 0;
     if (tid == 0) s_walk[0] = 0;
