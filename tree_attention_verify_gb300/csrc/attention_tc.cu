@@ -1065,7 +1065,7 @@ rd_attn_plan rd_attn_make_plan(bool causal, int B, int P_max, int Hq, int Hkv, i
     if (plan.tiles < 1) plan.tiles = 1;
     const long ctx_chunks = causal ? 1 : ((long)max_kv + kN - 1) / kN;
     const long base_units = (long)B * Hkv * plan.tiles;
-    const long target = 4L * 152;
+    const long target = 3L * 152;                         // split units wanted (GB300: 152 SMs)
     long cps = ctx_chunks > 0 ? ctx_chunks : 1;           // context chunks per split
     if (!causal && base_units < target && ctx_chunks > 4) {
         long want = (target + base_units - 1) / base_units;
