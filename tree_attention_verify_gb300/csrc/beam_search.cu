@@ -8,11 +8,12 @@
 // candidates (best first; equal scores go to the lower w*V + v) become the new
 // beams.  A beam whose score is -inf (not live yet) contributes no candidate.
 //
-// One thread-block cluster per request, one CTA per beam row (two rows per CTA
-// when W > 8).  Each CTA streams its row once with 16-byte loads, keeping the
-// running (max, sum of exponentials) and every thread's best W logits (higher
-// value first, lower token on ties); a CTA-wide selection then gives the row's
-// W best tokens, which are also its best candidates since the row's score
+// One thread-block cluster of up to four CTAs per request; CTA r takes beam
+// rows r, r + 4, ... (clusters of four with two rows per CTA measured faster
+// than one CTA per row at W = 8).  For each of its rows a CTA streams the row
+// with 16-byte loads for the running (max, sum of exponentials) and the
+// candidates, and selects the row's W best tokens (higher value first, lower
+// token on ties), which are also its best candidates since the row's score
 // offset scores_in[w] - lse[w] is common to them.  Rank 0 of the cluster reads
 // every row's log-sum-exp and W candidates from distributed shared memory and
 // picks the request's W best.  No CTA waits for another outside its cluster.
@@ -28,7 +29,7 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kNoIndex = 0x7fffffff;
-constexpr int kMaxCluster = 8;
+constexpr int kMaxCluster = 4;           // CTAs per request
 constexpr int kCap = 1024;                 // candidate slots per row
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
