@@ -76,12 +76,7 @@ extern "C" rd_status rd_greedy_accept_noalloc(const void* logits, int B, int P_m
         return RD_ERR_INVALID_ARG;
     void* scratch = nullptr;
     if (scratch_ptr(&scratch) != cudaSuccess) return RD_ERR_CUDA;
-    // the kernel expects keys [B*P_max] followed by tickets [B], all zero
-    unsigned long long* keys = static_cast<unsigned long long*>(scratch);
-    unsigned int* tickets = reinterpret_cast<unsigned int*>(
-        static_cast<unsigned char*>(scratch) + (size_t)B * P_max * sizeof(unsigned long long));
-    (void)keys;
-    (void)tickets;
+    // the kernel expects keys [B*P_max] (64-bit) followed by tickets [B] (32-bit), all zero
     cudaStream_t s = (cudaStream_t)stream;
     const size_t used = (size_t)B * P_max * sizeof(unsigned long long) + (size_t)B * sizeof(unsigned int);
     if (cudaMemsetAsync(scratch, 0, used, s) != cudaSuccess) return RD_ERR_CUDA;
