@@ -9,7 +9,7 @@ inputs resident in HBM.  Prints ONE JSON line (rank 0).
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 --impl reference times the fp64 CPU oracle (test infrastructure) on the host
-cores on a bounded sample of the same workload, scaled to the same metric.
+cores, one whole step of the same workload per timed step.
 For N > 1 (torchrun, one rank per GPU) every rank verifies its own batch
 (weak scaling, no collective on the data path); the step time is the maximum
 over ranks.
@@ -38,6 +38,7 @@ import workloads  # noqa: E402
 METRIC = "verify_steps_per_s"
 UNIT = "steps/s"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0          # GB300 HBM3e, nominal (context for the measured peak)
 ATTN_SRC = os.path.join(ROOT, "tree_attention_verify_gb300", "csrc", "attention_tc.cu")
 
 
@@ -52,7 +53,6 @@ def _args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="13b_b64", choices=list(workloads.CONFIGS))
     ap.add_argument("--e2e-steps", type=int, default=100)
-    ap.add_argument("--cpu-sample-requests", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-next-rows", action="store_true",
@@ -187,57 +187,58 @@ def attention_bytes(cfg, ctx_lens, packed_len) -> float:
 # ----------------------------------------------------------------------------
 # the oracle on the host cores (CPU baseline / reference arm)
 # ----------------------------------------------------------------------------
-def oracle_sample_time(inp, n_req: int, n_heads=None):
-    """Time the oracle on the first n_req requests (all kv heads unless n_heads is
-    given, then only the first n_heads kv heads of request 0).  Returns
-    (seconds, fraction of a full step that the sample covers, threads)."""
-    import oracle
+def oracle_host_inputs(inp, n_req=None) -> dict:
+    """Host copies (bf16 bit patterns) of the first n_req requests of one step's
+    inputs (all requests if None), made once, outside any timed region."""
     bits = workloads.bf16_bits
     cfg = inp["cfg"]
-    G = cfg.Hq // cfg.Hkv
-    offs = inp["ctx_offsets"].cpu().numpy()
-    n_req = max(1, min(n_req, cfg.B))
-    beams = inp["beams"][:n_req].cpu().numpy()
-    hs = cfg.Hkv if n_heads is None else max(1, min(n_heads, cfg.Hkv))
-    sub = dict(q=bits(inp["q"][:n_req, :, : hs * G]), kd=bits(inp["k_draft"][:n_req, :, :hs]),
-               vd=bits(inp["v_draft"][:n_req, :, :hs]),
-               kc=bits(inp["k_cache"][: int(offs[n_req]), :hs]),
-               vc=bits(inp["v_cache"][: int(offs[n_req]), :hs]),
-               logits=bits(inp["logits"][:n_req]), hidden=bits(inp["hidden"][:n_req]))
-    threads = oracle.n_threads_default()
-    oracle.build()
+    n_req = cfg.B if n_req is None else max(1, min(n_req, cfg.B))
+    offs = inp["ctx_offsets"].cpu().numpy()[: n_req + 1]
+    end = int(offs[-1])
+    return dict(cfg=cfg, n_req=n_req, offs=offs, beams=inp["beams"][:n_req].cpu().numpy(),
+                q=bits(inp["q"][:n_req]), kd=bits(inp["k_draft"][:n_req]),
+                vd=bits(inp["v_draft"][:n_req]), kc=bits(inp["k_cache"][:end]),
+                vc=bits(inp["v_cache"][:end]), logits=bits(inp["logits"][:n_req]),
+                hidden=bits(inp["hidden"][:n_req]))
+
+
+def oracle_step_time(h: dict, threads: int) -> float:
+    """Seconds of one oracle verification step over the requests in h: pack,
+    tree attention, greedy accept and unpack, as the GPU step runs them."""
+    import oracle
     t0 = time.perf_counter()
-    pk = oracle.oracle_pack(beams, cfg.P_max)
-    oracle.oracle_tree_attention(sub["q"], sub["kd"], sub["vd"], sub["kc"], sub["vc"],
-                                 offs[: n_req + 1], pk["packed_len"], pk["mask"],
-                                 n_threads=threads)
-    oracle.oracle_greedy_accept(sub["logits"], beams, pk["unpacker"], pk["packed_len"])
-    oracle.oracle_unpack(sub["hidden"], pk["unpacker"])
-    dt = time.perf_counter() - t0
-    frac = (n_req / cfg.B) * (hs / cfg.Hkv)
-    return dt, frac, threads
+    pk = oracle.oracle_pack(h["beams"], h["cfg"].P_max)
+    oracle.oracle_tree_attention(h["q"], h["kd"], h["vd"], h["kc"], h["vc"], h["offs"],
+                                 pk["packed_len"], pk["mask"], n_threads=threads)
+    oracle.oracle_greedy_accept(h["logits"], h["beams"], pk["unpacker"], pk["packed_len"])
+    oracle.oracle_unpack(h["hidden"], pk["unpacker"])
+    return time.perf_counter() - t0
 
 
 def run_reference(args):
+    """The oracle timed on the host cores: every timed step is one whole
+    verification step of the workload (all requests, all heads); each warm-up
+    step runs the first request only (it loads the library and touches the code;
+    a whole step there would only add minutes)."""
+    import oracle
     world, rank, _ = _dist()
     if rank != 0:
         return
     cfg = _config(args)
     inp = workloads.make_verify_inputs(cfg, device="cuda" if torch.cuda.is_available() else "cpu")
-    # size each step so that warmup + steps end within about two minutes
-    budget = 120.0 / max(1, args.steps + args.warmup)
-    probe_dt, probe_frac, threads = oracle_sample_time(inp, 1, n_heads=1)
-    n_heads = max(1, min(cfg.Hkv, int(budget / max(probe_dt, 1e-3))))
+    oracle.build()
+    threads = oracle.n_threads_default()
+    h_full = oracle_host_inputs(inp)
+    h_warm = oracle_host_inputs(inp, 1)
+    del inp
     for _ in range(args.warmup):
-        oracle_sample_time(inp, 1, n_heads=n_heads)
-    times, frac = [], None
-    for _ in range(args.steps):
-        dt, frac, threads = oracle_sample_time(inp, 1, n_heads=n_heads)
-        times.append(dt / frac)                 # seconds per full step
+        oracle_step_time(h_warm, threads)
+    times = [oracle_step_time(h_full, threads) for _ in range(args.steps)]
     step_s = statistics.mean(times)
     value = 1.0 / step_s
-    sample = (f"per step: request 0, {n_heads} of {cfg.Hkv} kv heads of tree attention plus its "
-              f"pack/accept/unpack, scaled by {1 / frac:.0f}x to a full {cfg.B}-request step")
+    sample = (f"every timed step is one whole {cfg.B}-request step (pack, tree attention, greedy "
+              f"accept, unpack) of the fp64 oracle on {threads} threads; warm-up steps run "
+              f"request 0 only")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -245,8 +246,8 @@ def run_reference(args):
             "config": {"workload": cfg.name, "B": cfg.B, "W": cfg.W, "L": cfg.L, "Hq": cfg.Hq,
                        "Hkv": cfg.Hkv, "D": cfg.D, "context": cfg.ctx[1], "vocab": cfg.vocab,
                        "Dh": cfg.Dh},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads,
+                             "host_cpus": os.cpu_count(), "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -270,6 +271,68 @@ def _time_us(fn, n: int = 20) -> float:
     return e0.elapsed_time(e1) / n * 1e3
 
 
+def _time_us_cold(fn, flush: torch.Tensor, n: int = 30) -> float:
+    """Mean device time of one call with L2 flushed before each call: the flush
+    (a write of a buffer larger than L2) runs outside the events around the call."""
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record()
+        fn()
+        e1.record()
+    torch.cuda.synchronize()
+    return statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs) * 1e3
+
+
+def measure_other_configs(dev, peak: float) -> dict:
+    """rd_tree_attention and rd_greedy_accept on the 8B-GQA serving batch and the
+    7B batch-1 workloads, each call timed with L2 flushed before it (their inputs
+    are smaller than or close to L2)."""
+    import tree_attention_verify_gb300 as rd
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)     # 256 MB
+    rows = {}
+    for name in ("8b_gqa_b16", "7b_b1"):
+        cfg = workloads.CONFIGS[name]
+        inp = workloads.make_verify_inputs(cfg, device=dev)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        pk = rd.rd_pack_beams(inp["beams"], cfg.P_max, dev_status=st)
+        max_ctx = int(inp["ctx_lens"].max())
+        n_ws = rd.rd_tree_attention_workspace_size(cfg.B, cfg.P_max, cfg.Hq, cfg.Hkv, cfg.D,
+                                                   max_ctx, dev)
+        ws = torch.zeros(max(16, n_ws), dtype=torch.uint8, device=dev)
+        o = torch.empty_like(inp["q"])
+        us = _time_us_cold(lambda: rd.rd_tree_attention(
+            inp["q"], inp["k_draft"], inp["v_draft"], inp["k_cache"], inp["v_cache"],
+            inp["ctx_offsets"], pk["packed_len"], pk["mask"], max_ctx=max_ctx, out=o,
+            workspace=ws, dev_status=st), flush)
+        plen = pk["packed_len"].cpu().numpy()
+        nb = attention_bytes(cfg, inp["ctx_lens"], plen)
+        wsa = torch.zeros(max(8, rd.rd_greedy_accept_workspace_size(cfg.B, cfg.P_max,
+                                                                    cfg.vocab)),
+                          dtype=torch.uint8, device=dev)
+        acc = rd.rd_greedy_accept(inp["logits"], inp["beams"], pk["unpacker"], pk["packed_len"],
+                                  workspace=wsa, dev_status=st)
+        us_acc = _time_us_cold(lambda: rd.rd_greedy_accept(
+            inp["logits"], inp["beams"], pk["unpacker"], pk["packed_len"], out=acc,
+            workspace=wsa, dev_status=st), flush)
+        acc_bytes = float(plen.sum()) * cfg.vocab * 2
+        torch.cuda.synchronize()
+        if int(st.item()) != 0:
+            raise SystemExit(f"device status {int(st.item())} on {name}")
+        rows[name] = {
+            "rd_tree_attention": {"us": us, "gbs": nb / us / 1e3, "frac": nb / us / 1e3 / peak,
+                                  "algorithmic_bytes": nb, "workspace_bytes": n_ws},
+            "rd_greedy_accept": {"us": us_acc, "gbs": acc_bytes / us_acc / 1e3,
+                                 "frac": acc_bytes / us_acc / 1e3 / peak},
+            "l2": "flushed before every timed call"}
+        del inp, o, ws
+    return rows
+
+
 def measure_next_rows(cfg, inp, step, dev, peak: float) -> dict:
     """The calls beyond the verification step, timed on the same workload's
     tensors after the timed region: FP8 and paged-cache attention, stochastic
@@ -280,7 +343,7 @@ def measure_next_rows(cfg, inp, step, dev, peak: float) -> dict:
     pk, acc = step.pk, step.acc
     max_ctx = max(1, int(inp["ctx_lens"].max()))
     ws = torch.zeros(max(16, rd.rd_tree_attention_workspace_size(
-        cfg.B, cfg.P_max, cfg.Hq, cfg.Hkv, cfg.D, max_ctx)), dtype=torch.uint8, device=dev)
+        cfg.B, cfg.P_max, cfg.Hq, cfg.Hkv, cfg.D, max_ctx, dev)), dtype=torch.uint8, device=dev)
     o = torch.empty_like(inp["q"])
     plen = pk["packed_len"].cpu().numpy()
     bf16_bytes = attention_bytes(cfg, inp["ctx_lens"], plen)
@@ -466,12 +529,15 @@ def run_ours(args):
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
                 "traffic": _profile_traffic(cfg.name),
-                "algorithmic_bytes_per_launch": attn_bytes}
+                "algorithmic_bytes_per_launch": attn_bytes,
+                "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
+                "nominal_peak": NOMINAL_HBM_GBS}
 
     next_rows = None
     if rank == 0 and not args.no_next_rows:
         next_rows = measure_next_rows(cfg, inp, step, dev, peak)
         next_rows["inflight_batch_8b"] = measure_mixed(dev)
+        next_rows["other_configs"] = measure_other_configs(dev, peak)
 
     # ---- end to end through the public API, host buffers ----------------------
     # Every step copies its inputs from pinned host memory and reads its accepted
@@ -537,12 +603,17 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n_req = args.cpu_sample_requests
-        dt, frac, threads = oracle_sample_time(inp, n_req)
-        cpu = {"value": frac / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": f"first {max(1, min(n_req, cfg.B))} of {cfg.B} requests of one step "
-                         f"(pack, tree attention, greedy accept, unpack), {dt:.1f} s, scaled "
-                         f"to a full step"}
+        import oracle
+        oracle.build()
+        threads = oracle.n_threads_default()
+        h = oracle_host_inputs(inp)
+        dt = oracle_step_time(h, threads)
+        del h
+        cpu = {"value": 1.0 / dt, "unit": UNIT, "cores": threads, "host_cpus": os.cpu_count(),
+               "kind": "oracle",
+               "sample": f"one whole step of the workload ({cfg.B} requests: pack, tree "
+                         f"attention, greedy accept, unpack) of the fp64 oracle, {dt:.1f} s, "
+                         f"not scaled"}
 
     if rank == 0:
         line = {

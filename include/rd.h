@@ -132,8 +132,11 @@ rd_status rd_pack_beams(const int32_t* beams, int B, int W, int L, int P_cap,
  * scale      softmax scale; <= 0 selects 1/sqrt(D)
  * workspace  device scratch of rd_tree_attention_workspace_size() bytes
  *            (split-KV partials and merge tickets).  It must be zero-filled
- *            before its first use; every call leaves its tickets at zero again.
- *            Calls that share a workspace must not overlap in time.
+ *            before its first use; every call leaves its tickets at zero again
+ *            (except a call that set RD_DEV_TIMEOUT: zero it again after one).
+ *            Calls that share a workspace must not overlap in time.  The size
+ *            depends on the SM count of the current device: query it with the
+ *            device current that the call will run on.
  * Supported: D in {64, 128}; Hq % Hkv == 0; 1 <= P_max <= RD_MAX_PACKED.
  */
 size_t rd_tree_attention_workspace_size(int B, int P_max, int Hq, int Hkv, int D,
@@ -325,6 +328,23 @@ rd_status rd_greedy_accept(const void* logits, int B, int P_max, int V,
                            int32_t* dev_status, rd_stream_t stream);
 
 /*
+ * rd_debug_stall_attention -- failure-detection test hook.  The pages have no
+ * counterpart: it exists to test the kernels' bounded waits without a GPU fault.
+ *
+ * budget_cycles > 0 arms it for every later rd_tree_attention,
+ * rd_tree_attention_paged, rd_tree_attention_fp8 and rd_causal_attention
+ * launch of this process: before its first MMA, each CTA's MMA-issuing thread
+ * waits on a barrier that nothing completes, for at most budget_cycles SM
+ * clock cycles.  That wait runs out, the CTA records RD_DEV_TIMEOUT, its other
+ * roles stop at their next wait, it waits (with the normal budget) for the
+ * copies and MMAs it has issued, frees its tensor memory and returns.  The
+ * outputs of such a launch are undefined, and its split-KV workspace must be
+ * zeroed again.  budget_cycles <= 0 disarms it (the default).  Process-wide;
+ * do not arm it while other threads launch attention they rely on.
+ */
+void rd_debug_stall_attention(long long budget_cycles);
+
+/*
  * rd_greedy_accept_noalloc -- rd_greedy_accept for callers that cannot
  * allocate device memory.  The pages have no counterpart: this is a library
  * convenience, not part of the method.
@@ -346,7 +366,10 @@ rd_status rd_greedy_accept(const void* logits, int B, int P_max, int V,
  *    give wrong results.  Order them on one stream.
  *  - The first call on a device looks the array's device address up with that
  *    device current (cudaGetSymbolAddress); make that first call before any
- *    stream capture begins.
+ *    stream capture begins.  The address is kept for the life of the process:
+ *    after a cudaDeviceReset of that device it is stale, so do not call this
+ *    entry point on a device that has been reset.
+ *  - All tensors must be on the current device.
  */
 rd_status rd_greedy_accept_noalloc(const void* logits, int B, int P_max, int V,
                                    const int32_t* beams, const int32_t* unpacker,

@@ -115,3 +115,42 @@ def test_commit_accepted_matches_oracle(name):
     np.testing.assert_array_equal(new_lens.cpu().numpy(), lens_ref)
     np.testing.assert_array_equal(bf16_bits(pg["k_pool"]), k_ref)
     np.testing.assert_array_equal(bf16_bits(pg["v_pool"]), v_ref)
+
+
+def test_paged_attention_13b_full_size_sampled():
+    # The 13B-shaped batch at full size (64 requests, 40 heads, 8192-position
+    # contexts) in 256-position pages of a shuffled pool; sampled (request, kv
+    # head) pairs against the oracle, each given the request's own pages (in a
+    # shuffled sub-pool with a renumbered block table) and that head.
+    rd = _rd()
+    cfg = workloads.CONFIGS["13b_b64"]
+    inp, pg = _paged_inputs(cfg, None, 256, seed=3)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pk = rd.rd_pack_beams(inp["beams"], cfg.P_max, dev_status=st)
+    o = rd.rd_tree_attention_paged(inp["q"], inp["k_draft"], inp["v_draft"], pg["k_pool"],
+                                   pg["v_pool"], pg["block_table"], pg["ctx_lens"],
+                                   pk["packed_len"], pk["mask"], max_ctx=8192, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    pk_ref = oracle.oracle_pack(inp["beams"].cpu().numpy(), cfg.P_max)
+    got = o.float().cpu().numpy()
+    table = pg["block_table"].cpu().numpy()
+    lens = pg["ctx_lens"].cpu().numpy()
+    rng = np.random.default_rng(23)
+    sample = [(0, 0), (63, 39)] + [(int(rng.integers(64)), int(rng.integers(40)))
+                                   for _ in range(6)]
+    for b, h in sample:
+        n_b = -(-int(lens[b]) // 256)
+        pages = table[b, :n_b].astype(np.int64)
+        perm = rng.permutation(n_b)                      # sub-pool slot of each page
+        sub_k = torch.empty((n_b, 256, 1, cfg.D), dtype=torch.bfloat16, device=DEV)
+        sub_v = torch.empty_like(sub_k)
+        idx = torch.from_numpy(pages).to(DEV)
+        sub_k[torch.from_numpy(perm).to(DEV)] = pg["k_pool"][idx, :, h:h + 1]
+        sub_v[torch.from_numpy(perm).to(DEV)] = pg["v_pool"][idx, :, h:h + 1]
+        sub_table = perm.astype(np.int32)[None, :]
+        ref = oracle.oracle_tree_attention_paged(
+            bf16_bits(inp["q"][b:b + 1, :, h:h + 1]), bf16_bits(inp["k_draft"][b:b + 1, :, h:h + 1]),
+            bf16_bits(inp["v_draft"][b:b + 1, :, h:h + 1]), bf16_bits(sub_k), bf16_bits(sub_v),
+            sub_table, lens[b:b + 1], pk_ref["packed_len"][b:b + 1], pk_ref["mask"][b:b + 1])
+        _close(got[b:b + 1, :, h:h + 1], ref, f"paged 13B b={b} h={h}")

@@ -462,3 +462,52 @@ def test_tree_attention_reused_workspace_split_launches():
             bf16_bits(inp["v_cache"][sl, h:h + 1]), np.array([0, offs[b + 1] - offs[b]], np.int64),
             pk_ref["packed_len"][b:b + 1], pk_ref["mask"][b:b + 1])
         _close(got[b:b + 1, :, hs], ref, f"{cfg.name} b={b} h={h}")
+
+
+@pytest.mark.parametrize("split", ["mixed", "all_ctx", "all_gen"])
+def test_mixed_batch_full_size(split):
+    # The in-flight batch at its stated size: 32 requests on 8B-GQA shapes, each a
+    # 512-token causal prefill chunk or a W=8, L=5 verification over a context of
+    # 512..8192 positions (G = 4).  Context half: every sequence against the oracle
+    # and its greedy token bit-exact.  Generation half: pack and greedy acceptance
+    # bit-exact for every request; attention on sampled (request, kv head) pairs
+    # that include the longest context; unpack bit-exact.
+    rd = _rd()
+    m = workloads.make_mixed_inputs(split, device=DEV)
+    st = _status()
+    c, n_ctx = m["ctx"], m["n_ctx"]
+    if n_ctx:
+        oc = rd.rd_causal_attention(c["q"], c["k"], c["v"], c["cu_seqlens"],
+                                    max_seqlen=m["prefill_len"], dev_status=st)
+        one = torch.zeros((n_ctx, 1, 1), dtype=torch.int32, device=DEV)
+        acc_c = rd.rd_greedy_accept(c["logits"], one, one,
+                                    torch.ones(n_ctx, dtype=torch.int32, device=DEV),
+                                    dev_status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        ref = oracle.oracle_causal_attention(bf16_bits(c["q"]), bf16_bits(c["k"]),
+                                             bf16_bits(c["v"]), c["cu_seqlens"].cpu().numpy())
+        _close(oc.float().cpu().numpy(), ref, f"{split}: context half")
+        lg = bf16_bits(c["logits"])
+        g = np.argmax((lg.astype(np.uint32) << 16).view(np.float32), -1)
+        np.testing.assert_array_equal(acc_c["out_tokens"].cpu().numpy()[:, 0], g[:, 0])
+    if m["n_gen"]:
+        g_inp = m["gen"]
+        cfg = g_inp["cfg"]
+        lens = np.asarray(g_inp["ctx_lens"])
+        rng = np.random.default_rng(17)
+        longest = int(np.argmax(lens))
+        sample = [(longest, 0), (longest, cfg.Hkv - 1), (int(np.argmin(lens)), 3)]
+        sample += [(int(rng.integers(cfg.B)), int(rng.integers(cfg.Hkv))) for _ in range(6)]
+        _attention_case(g_inp, sample_bh=sample)
+        assert lens.max() > 7000
+        pk = rd.rd_pack_beams(g_inp["beams"], cfg.P_max, dev_status=st)
+        acc = rd.rd_greedy_accept(g_inp["logits"], g_inp["beams"], pk["unpacker"],
+                                  pk["packed_len"], dev_status=st)
+        hid = rd.rd_unpack(g_inp["hidden"], pk["unpacker"], dev_status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        pk_ref = oracle.oracle_pack(g_inp["beams"].cpu().numpy(), cfg.P_max)
+        _accept_check(g_inp, pk_ref, acc)
+        np.testing.assert_array_equal(bf16_bits(hid), oracle.oracle_unpack(
+            bf16_bits(g_inp["hidden"]), pk_ref["unpacker"]))

@@ -6,20 +6,23 @@ Runs last (file name) so that a stop at the first failure has already run every
 other test.  It must pass both alone in a fresh process and after the others.
 """
 import ctypes
+import dataclasses
 
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads
+from workloads import bf16_bits
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
 
 
-def _inputs(name, seed_offset=0):
+def _inputs(name, seed_offset=0, cfg=None):
     import tree_attention_verify_gb300 as rd
-    cfg = workloads.CONFIGS[name]
+    cfg = workloads.CONFIGS[name] if cfg is None else cfg
     rng = np.random.default_rng(cfg.seed + seed_offset)
     gen = torch.Generator(device=DEV).manual_seed(cfg.seed + seed_offset)
     trees = workloads.draft_trees(cfg.B, cfg.W, cfg.L, cfg.vocab, cfg.share, rng)
@@ -65,6 +68,36 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
         for k in ref:
             np.testing.assert_array_equal(got[k].cpu().numpy(), ref[k].cpu().numpy(),
                                           err_msg=f"{name}: {k}")
+        _check_oracle(got, logits, beams, unpacker, packed_len, name)
+
+
+def _check_oracle(got, logits, beams, unpacker, packed_len, what):
+    # the fp64 oracle of greedy verification decides the same integers
+    ref = oracle.oracle_greedy_accept(bf16_bits(logits), beams.cpu().numpy(),
+                                      unpacker.cpu().numpy(), packed_len.cpu().numpy())
+    for k in ref:
+        np.testing.assert_array_equal(got[k].cpu().numpy(), ref[k], err_msg=f"{what}: {k}")
+
+
+def test_noalloc_wrapper_at_the_scratch_limit():
+    # B * P_max == 65536 keys: the whole key array and the tickets behind it are
+    # used; two calls in a row through the Python binding, each against the
+    # workspace entry point and the oracle
+    import tree_attention_verify_gb300 as rd
+    cfg = dataclasses.replace(workloads.CONFIGS["8b_gqa_b16"], B=1024, W=8, L=8, vocab=512,
+                              name="noalloc_limit")
+    assert cfg.B * cfg.P_max == 65536
+    for off in (0, 1):
+        logits, beams, unpacker, packed_len = _inputs(None, off, cfg)
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        got = rd.rd_greedy_accept_noalloc(logits, beams, unpacker, packed_len, dev_status=st)
+        ref = rd.rd_greedy_accept(logits, beams, unpacker, packed_len)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        for k in ref:
+            np.testing.assert_array_equal(got[k].cpu().numpy(), ref[k].cpu().numpy(),
+                                          err_msg=f"limit call {off}: {k}")
+        _check_oracle(got, logits, beams, unpacker, packed_len, f"limit call {off}")
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
@@ -76,4 +109,9 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     one = ctypes.c_void_p(256)
     # 300 requests x 256 packed rows = 76800 keys > 65536
     assert fn(one, 300, 256, 1000, one, one, one, 4, 4, one, one, one, one, one, None,
+              None) == rd.RD_ERR_UNSUPPORTED
+    # one key past the array: 1025 x 64 = 65600, and 65537 requests of one row
+    assert fn(one, 1025, 64, 1000, one, one, one, 8, 8, one, one, one, one, one, None,
+              None) == rd.RD_ERR_UNSUPPORTED
+    assert fn(one, 65537, 1, 1000, one, one, one, 1, 1, one, one, one, one, one, None,
               None) == rd.RD_ERR_UNSUPPORTED

@@ -4,7 +4,8 @@ unpack).
 
 The binding only marshals arguments: it checks tensor shapes, dtypes, devices
 and contiguity, allocates outputs with torch when the caller passes none, and
-calls the C ABI declared in include/rd.h on the current CUDA stream.  Every step
+calls the C ABI declared in include/rd.h with the tensors' device current, on
+that device's current CUDA stream (or the stream passed).  Every step
 of the computation runs in the CUDA kernels of librd.so.  There is no CPU path:
 if the library cannot be loaded, importing this package raises.
 """
@@ -23,8 +24,9 @@ __all__ = [
     "rd_causal_attention", "rd_unpack", "rd_greedy_accept",
     "rd_greedy_accept_workspace_size", "rd_greedy_accept_noalloc",
     "rd_tree_attention_paged", "rd_commit_accepted", "rd_beam_search_step",
-    "rd_tree_attention_fp8", "RdError", "DEV_BAD_INDEX", "DEV_BAD_TOKEN",
-    "DEV_OVERFLOW", "DEV_BAD_LENGTH", "DEV_TIMEOUT", "lib_path",
+    "rd_tree_attention_fp8", "rd_sample_accept", "rd_debug_stall_attention", "RdError",
+    "DEV_BAD_INDEX", "DEV_BAD_TOKEN", "DEV_OVERFLOW", "DEV_BAD_LENGTH", "DEV_TIMEOUT",
+    "lib_path",
 ]
 
 DEV_BAD_INDEX, DEV_BAD_TOKEN, DEV_OVERFLOW, DEV_BAD_LENGTH, DEV_TIMEOUT = 1, 2, 4, 8, 16
@@ -71,6 +73,8 @@ def _load() -> ctypes.CDLL:
         f.restype = S if name.endswith("workspace_size") else I
     lib.rd_status_string.argtypes = [I]
     lib.rd_status_string.restype = ctypes.c_char_p
+    lib.rd_debug_stall_attention.argtypes = [ctypes.c_longlong]
+    lib.rd_debug_stall_attention.restype = None
     return lib
 
 
@@ -88,8 +92,8 @@ def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _stream(stream) -> ctypes.c_void_p:
-    s = torch.cuda.current_stream() if stream is None else stream
+def _stream(stream, device=None) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream(device) if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
 
 
@@ -113,8 +117,50 @@ def _check(fn: str, status: int):
         raise RdError(fn, status)
 
 
+def _run(name: str, like: torch.Tensor, *args, stream=None):
+    """Call librd's `name` with `like`'s device current and that device's
+    stream (or `stream`) as the last argument; raise RdError on a bad status."""
+    with torch.cuda.device(like.device):
+        _check(name, getattr(_lib, name)(*args, _stream(stream, like.device)))
+
+
 def _empty(shape, dtype, like: torch.Tensor):
     return torch.empty(shape, dtype=dtype, device=like.device)
+
+
+_ACCEPT_OUTS = ("argmax", "accept_len", "best_beam", "n_accepted", "out_tokens")
+
+
+def _accept_shapes(logits, beams, unpacker, packed_len, out=None) -> dict:
+    """Shapes of the greedy-verification arguments, checked against each other
+    before anything is launched: a batch or beam count that disagrees between
+    logits, beams, unpacker, packed_len and the outputs would make the kernel
+    index outside those tensors.  Returns the expected output shapes."""
+    if logits.dim() != 3:
+        raise ValueError(f"logits must be [B, P_max, V], got {tuple(logits.shape)}")
+    B, P, _ = logits.shape
+    if beams.dim() != 3 or beams.shape[0] != B:
+        raise ValueError(f"beams must be [B={B}, W, L], got {tuple(beams.shape)}")
+    W, L = beams.shape[1], beams.shape[2]
+    if tuple(unpacker.shape) != tuple(beams.shape):
+        raise ValueError(f"unpacker must have the shape of beams {tuple(beams.shape)}, "
+                         f"got {tuple(unpacker.shape)}")
+    if packed_len.dim() != 1 or packed_len.numel() != B:
+        raise ValueError(f"packed_len must be [B={B}], got {tuple(packed_len.shape)}")
+    shapes = dict(argmax=(B, P), accept_len=(B, W), best_beam=(B,), n_accepted=(B,),
+                  out_tokens=(B, L))
+    if out is not None:
+        for k in _ACCEPT_OUTS:
+            t = out.get(k)
+            if not isinstance(t, torch.Tensor):
+                raise TypeError(f"out[{k!r}] must be a tensor")
+            if tuple(t.shape) != shapes[k]:
+                raise ValueError(f"out[{k!r}] must be {shapes[k]}, got {tuple(t.shape)}")
+            if t.dtype != torch.int32 or not t.is_contiguous():
+                raise ValueError(f"out[{k!r}] must be a contiguous int32 tensor")
+            if t.device != logits.device:
+                raise ValueError(f"out[{k!r}] is on {t.device}, expected {logits.device}")
+    return shapes
 
 
 # ----------------------------------------------------------------------------
@@ -135,15 +181,20 @@ def rd_pack_beams(beams: torch.Tensor, P_cap: Optional[int] = None, *, out: Opti
                    mask=_empty((B, P_cap, NW), torch.int32, beams),   # uint32 bit rows
                    depth=_empty((B, P_cap), torch.int32, beams),
                    packed_len=_empty((B,), torch.int32, beams))
-    _check("rd_pack_beams", _lib.rd_pack_beams(
+    _run("rd_pack_beams", beams,
         _ptr(beams), B, W, L, P_cap, _ptr(out["tokens"]), _ptr(out["packer"]),
         _ptr(out["unpacker"]), _ptr(out["mask"]), _ptr(out.get("depth")),
-        _ptr(out["packed_len"]), _ptr(dev_status), _stream(stream)))
+        _ptr(out["packed_len"]), _ptr(dev_status), stream=stream)
     return out
 
 
 def rd_tree_attention_workspace_size(B: int, P_max: int, Hq: int, Hkv: int, D: int,
-                                     max_ctx: int) -> int:
+                                     max_ctx: int, device=None) -> int:
+    """Bytes of split-KV workspace; it depends on the SM count of the device the
+    call will run on (`device`, else the current device)."""
+    if device is not None and torch.device(device).type == "cuda":
+        with torch.cuda.device(device):
+            return int(_lib.rd_tree_attention_workspace_size(B, P_max, Hq, Hkv, D, max_ctx))
     return int(_lib.rd_tree_attention_workspace_size(B, P_max, Hq, Hkv, D, max_ctx))
 
 
@@ -156,13 +207,14 @@ def rd_tree_attention(q, k_new, v_new, k_cache, v_cache, ctx_offsets, packed_len
     The workspace (if the plan needs one) must start zero-filled; it is returned
     to zero by every call.  Pass the same workspace again to reuse it."""
     for n, t in (("q", q), ("k_new", k_new), ("v_new", v_new)):
-        _need(t, n, torch.bfloat16, ndim=4)
-    _need(k_cache, "k_cache", torch.bfloat16, ndim=3)
-    _need(v_cache, "v_cache", torch.bfloat16, ndim=3)
-    _need(ctx_offsets, "ctx_offsets", torch.int64, ndim=1)
-    _need(packed_len, "packed_len", torch.int32, ndim=1)
-    if mask.dim() != 3 or not mask.is_contiguous() or mask.element_size() != 4:
-        raise ValueError("mask must be a contiguous 32-bit [B, P_max, NW] tensor")
+        _need(t, n, torch.bfloat16, q.device, ndim=4)
+    _need(k_cache, "k_cache", torch.bfloat16, q.device, ndim=3)
+    _need(v_cache, "v_cache", torch.bfloat16, q.device, ndim=3)
+    _need(ctx_offsets, "ctx_offsets", torch.int64, q.device, ndim=1)
+    _need(packed_len, "packed_len", torch.int32, q.device, ndim=1)
+    if (mask.dim() != 3 or not mask.is_contiguous() or mask.element_size() != 4
+            or mask.device != q.device):
+        raise ValueError("mask must be a contiguous 32-bit [B, P_max, NW] tensor on q's device")
     B, P, Hq, D = q.shape
     Hkv = k_new.shape[2]
     if k_new.shape != (B, P, Hkv, D) or v_new.shape != k_new.shape:
@@ -173,15 +225,15 @@ def rd_tree_attention(q, k_new, v_new, k_cache, v_cache, ctx_offsets, packed_len
         raise ValueError("ctx_offsets/packed_len/mask shapes do not match q")
     if out is None:
         out = torch.empty_like(q)
-    ws_need = rd_tree_attention_workspace_size(B, P, Hq, Hkv, D, max_ctx)
+    ws_need = rd_tree_attention_workspace_size(B, P, Hq, Hkv, D, max_ctx, q.device)
     if ws_need and workspace is None:
         workspace = torch.zeros(ws_need, dtype=torch.uint8, device=q.device)
-    _check("rd_tree_attention", _lib.rd_tree_attention(
+    _run("rd_tree_attention", q,
         B, P, Hq, Hkv, D, float(scale), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
         _ptr(v_cache), _ptr(ctx_offsets), int(k_cache.shape[0]), int(max_ctx), _ptr(packed_len),
         _ptr(mask), int(mask.shape[2]), _ptr(out), _ptr(workspace),
         0 if workspace is None else workspace.numel() * workspace.element_size(),
-        _ptr(dev_status), _stream(stream)))
+        _ptr(dev_status), stream=stream)
     return out
 
 
@@ -192,31 +244,38 @@ def rd_tree_attention_fp8(q, k_new, v_new, k_cache, v_cache, k_scale: float, v_s
     float8_e4m3fn) [total_ctx, Hkv, D] holding e4m3 bit patterns, per-tensor
     scales k_scale/v_scale (see rd_tree_attention_fp8 in rd.h)."""
     for n, t in (("q", q), ("k_new", k_new), ("v_new", v_new)):
-        _need(t, n, torch.bfloat16, ndim=4)
+        _need(t, n, torch.bfloat16, q.device, ndim=4)
     if k_cache.dtype != torch.uint8:
         k_cache = k_cache.view(torch.uint8)
     if v_cache.dtype != torch.uint8:
         v_cache = v_cache.view(torch.uint8)
-    _need(k_cache, "k_cache", torch.uint8, ndim=3)
-    _need(v_cache, "v_cache", torch.uint8, ndim=3)
-    _need(ctx_offsets, "ctx_offsets", torch.int64, ndim=1)
-    _need(packed_len, "packed_len", torch.int32, ndim=1)
+    _need(k_cache, "k_cache", torch.uint8, q.device, ndim=3)
+    _need(v_cache, "v_cache", torch.uint8, q.device, ndim=3)
+    _need(ctx_offsets, "ctx_offsets", torch.int64, q.device, ndim=1)
+    _need(packed_len, "packed_len", torch.int32, q.device, ndim=1)
+    if (mask.dim() != 3 or not mask.is_contiguous() or mask.element_size() != 4
+            or mask.device != q.device):
+        raise ValueError("mask must be a contiguous 32-bit [B, P_max, NW] tensor on q's device")
     B, P, Hq, D = q.shape
     Hkv = k_new.shape[2]
+    if k_new.shape != (B, P, Hkv, D) or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new must be [B, P_max, Hkv, D]")
     if k_cache.shape[1:] != (Hkv, D) or v_cache.shape != k_cache.shape:
         raise ValueError("k_cache/v_cache must be [total_ctx, Hkv, D]")
+    if ctx_offsets.numel() != B + 1 or packed_len.numel() != B or mask.shape[:2] != (B, P):
+        raise ValueError("ctx_offsets/packed_len/mask shapes do not match q")
     if out is None:
         out = torch.empty_like(q)
-    ws_need = rd_tree_attention_workspace_size(B, P, Hq, Hkv, D, max_ctx)
+    ws_need = rd_tree_attention_workspace_size(B, P, Hq, Hkv, D, max_ctx, q.device)
     if ws_need and workspace is None:
         workspace = torch.zeros(ws_need, dtype=torch.uint8, device=q.device)
-    _check("rd_tree_attention_fp8", _lib.rd_tree_attention_fp8(
+    _run("rd_tree_attention_fp8", q,
         B, P, Hq, Hkv, D, float(scale), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
         _ptr(v_cache), float(k_scale), float(v_scale), _ptr(ctx_offsets),
         int(k_cache.shape[0]), int(max_ctx), _ptr(packed_len), _ptr(mask), int(mask.shape[2]),
         _ptr(out), _ptr(workspace),
         0 if workspace is None else workspace.numel() * workspace.element_size(),
-        _ptr(dev_status), _stream(stream)))
+        _ptr(dev_status), stream=stream)
     return out
 
 
@@ -227,14 +286,15 @@ def rd_tree_attention_paged(q, k_new, v_new, k_pool, v_pool, block_table, ctx_le
     [num_pages, page_size, Hkv, D] bf16, block_table int32 [B, max_pages],
     ctx_lens int32 [B] (see rd_tree_attention_paged in rd.h)."""
     for n, t in (("q", q), ("k_new", k_new), ("v_new", v_new)):
-        _need(t, n, torch.bfloat16, ndim=4)
-    _need(k_pool, "k_pool", torch.bfloat16, ndim=4)
-    _need(v_pool, "v_pool", torch.bfloat16, ndim=4)
-    _need(block_table, "block_table", torch.int32, ndim=2)
-    _need(ctx_lens, "ctx_lens", torch.int32, ndim=1)
-    _need(packed_len, "packed_len", torch.int32, ndim=1)
-    if mask.dim() != 3 or not mask.is_contiguous() or mask.element_size() != 4:
-        raise ValueError("mask must be a contiguous 32-bit [B, P_max, NW] tensor")
+        _need(t, n, torch.bfloat16, q.device, ndim=4)
+    _need(k_pool, "k_pool", torch.bfloat16, q.device, ndim=4)
+    _need(v_pool, "v_pool", torch.bfloat16, q.device, ndim=4)
+    _need(block_table, "block_table", torch.int32, q.device, ndim=2)
+    _need(ctx_lens, "ctx_lens", torch.int32, q.device, ndim=1)
+    _need(packed_len, "packed_len", torch.int32, q.device, ndim=1)
+    if (mask.dim() != 3 or not mask.is_contiguous() or mask.element_size() != 4
+            or mask.device != q.device):
+        raise ValueError("mask must be a contiguous 32-bit [B, P_max, NW] tensor on q's device")
     B, P, Hq, D = q.shape
     Hkv = k_new.shape[2]
     n_pages, page_size = k_pool.shape[0], k_pool.shape[1]
@@ -244,16 +304,16 @@ def rd_tree_attention_paged(q, k_new, v_new, k_pool, v_pool, block_table, ctx_le
         raise ValueError("block_table/ctx_lens/packed_len do not match the batch")
     if out is None:
         out = torch.empty_like(q)
-    ws_need = rd_tree_attention_workspace_size(B, P, Hq, Hkv, D, max_ctx)
+    ws_need = rd_tree_attention_workspace_size(B, P, Hq, Hkv, D, max_ctx, q.device)
     if ws_need and workspace is None:
         workspace = torch.zeros(ws_need, dtype=torch.uint8, device=q.device)
-    _check("rd_tree_attention_paged", _lib.rd_tree_attention_paged(
+    _run("rd_tree_attention_paged", q,
         B, P, Hq, Hkv, D, float(scale), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool),
         _ptr(v_pool), n_pages, page_size, _ptr(block_table), block_table.shape[1],
         _ptr(ctx_lens), int(max_ctx), _ptr(packed_len), _ptr(mask), int(mask.shape[2]),
         _ptr(out), _ptr(workspace),
         0 if workspace is None else workspace.numel() * workspace.element_size(),
-        _ptr(dev_status), _stream(stream)))
+        _ptr(dev_status), stream=stream)
     return out
 
 
@@ -263,21 +323,21 @@ def rd_commit_accepted(k_new, v_new, unpacker, best_beam, n_accepted, k_pool, v_
     """Append the accepted path's K/V to the paged cache (k_pool/v_pool modified in
     place).  Returns new_ctx_lens = ctx_lens + n_accepted + 1 (see rd.h)."""
     _need(k_new, "k_new", torch.bfloat16, ndim=4)
-    _need(v_new, "v_new", torch.bfloat16, ndim=4)
-    _need(k_pool, "k_pool", torch.bfloat16, ndim=4)
-    _need(v_pool, "v_pool", torch.bfloat16, ndim=4)
+    _need(v_new, "v_new", torch.bfloat16, k_new.device, ndim=4)
+    _need(k_pool, "k_pool", torch.bfloat16, k_new.device, ndim=4)
+    _need(v_pool, "v_pool", torch.bfloat16, k_new.device, ndim=4)
     for n, t in (("unpacker", unpacker), ("best_beam", best_beam), ("n_accepted", n_accepted),
                  ("block_table", block_table), ("ctx_lens", ctx_lens)):
-        _need(t, n, torch.int32)
+        _need(t, n, torch.int32, k_new.device)
     B, P, Hkv, D = k_new.shape
     _, W, L = unpacker.shape
     if new_ctx_lens is None:
         new_ctx_lens = torch.empty_like(ctx_lens)
-    _check("rd_commit_accepted", _lib.rd_commit_accepted(
+    _run("rd_commit_accepted", k_new,
         B, W, L, P, Hkv, D, _ptr(k_new), _ptr(v_new), _ptr(unpacker), _ptr(best_beam),
         _ptr(n_accepted), _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], k_pool.shape[1],
         _ptr(block_table), block_table.shape[1], _ptr(ctx_lens), _ptr(new_ctx_lens),
-        _ptr(dev_status), _stream(stream)))
+        _ptr(dev_status), stream=stream)
     return new_ctx_lens
 
 
@@ -285,17 +345,17 @@ def rd_causal_attention(q, k, v, cu_seqlens, *, max_seqlen: int, scale: float = 
                         out=None, dev_status=None, stream=None) -> torch.Tensor:
     """Causal prefill attention: q [T,Hq,D], k/v [T,Hkv,D] bf16, cu_seqlens int32 [B+1]."""
     _need(q, "q", torch.bfloat16, ndim=3)
-    _need(k, "k", torch.bfloat16, ndim=3)
-    _need(v, "v", torch.bfloat16, ndim=3)
-    _need(cu_seqlens, "cu_seqlens", torch.int32, ndim=1)
+    _need(k, "k", torch.bfloat16, q.device, ndim=3)
+    _need(v, "v", torch.bfloat16, q.device, ndim=3)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, q.device, ndim=1)
     T, Hq, D = q.shape
     if k.shape[0] != T or v.shape != k.shape or k.shape[2] != D:
         raise ValueError("k/v must be [T, Hkv, D] with the rows of q")
     if out is None:
         out = torch.empty_like(q)
-    _check("rd_causal_attention", _lib.rd_causal_attention(
+    _run("rd_causal_attention", q,
         cu_seqlens.numel() - 1, Hq, k.shape[1], D, float(scale), _ptr(q), _ptr(k), _ptr(v),
-        _ptr(cu_seqlens), T, int(max_seqlen), _ptr(out), _ptr(dev_status), _stream(stream)))
+        _ptr(cu_seqlens), T, int(max_seqlen), _ptr(out), _ptr(dev_status), stream=stream)
     return out
 
 
@@ -305,16 +365,15 @@ def rd_unpack(packed: torch.Tensor, unpacker: torch.Tensor, *, out=None, dev_sta
     if packed.dtype not in _DTYPES:
         raise TypeError(f"unsupported dtype {packed.dtype}")
     _need(packed, "packed", packed.dtype, ndim=3)
-    _need(unpacker, "unpacker", torch.int32, ndim=3)
+    _need(unpacker, "unpacker", torch.int32, packed.device, ndim=3)
     B, P, Dh = packed.shape
     _, W, L = unpacker.shape
     if unpacker.shape[0] != B:
         raise ValueError("unpacker batch does not match packed")
     if out is None:
         out = _empty((B, W, L, Dh), packed.dtype, packed)
-    _check("rd_unpack", _lib.rd_unpack(_ptr(packed), _DTYPES[packed.dtype], B, P, Dh,
-                                       _ptr(unpacker), W, L, _ptr(out), _ptr(dev_status),
-                                       _stream(stream)))
+    _run("rd_unpack", packed, _ptr(packed), _DTYPES[packed.dtype], B, P, Dh, _ptr(unpacker), W,
+         L, _ptr(out), _ptr(dev_status), stream=stream)
     return out
 
 
@@ -327,26 +386,26 @@ def rd_greedy_accept(logits, beams, unpacker, packed_len, *, out=None, workspace
     """Greedy verification (see rd_greedy_accept in rd.h).  Returns dict(argmax,
     accept_len, best_beam, n_accepted, out_tokens).  The workspace must start
     zero-filled; every call leaves it zeroed."""
+    shapes = _accept_shapes(logits, beams, unpacker, packed_len, out)
+    dev = logits.device
     _need(logits, "logits", torch.bfloat16, ndim=3)
-    _need(beams, "beams", torch.int32, ndim=3)
-    _need(unpacker, "unpacker", torch.int32, ndim=3)
-    _need(packed_len, "packed_len", torch.int32, ndim=1)
+    _need(beams, "beams", torch.int32, dev, ndim=3)
+    _need(unpacker, "unpacker", torch.int32, dev, ndim=3)
+    _need(packed_len, "packed_len", torch.int32, dev, ndim=1)
     B, P, V = logits.shape
     _, W, L = beams.shape
     if out is None:
-        out = dict(argmax=_empty((B, P), torch.int32, logits),
-                   accept_len=_empty((B, W), torch.int32, logits),
-                   best_beam=_empty((B,), torch.int32, logits),
-                   n_accepted=_empty((B,), torch.int32, logits),
-                   out_tokens=_empty((B, L), torch.int32, logits))
+        out = {k: _empty(shapes[k], torch.int32, logits) for k in _ACCEPT_OUTS}
     if workspace is None:
         workspace = torch.zeros(max(8, rd_greedy_accept_workspace_size(B, P, V)),
-                                dtype=torch.uint8, device=logits.device)
-    _check("rd_greedy_accept", _lib.rd_greedy_accept(
-        _ptr(logits), B, P, V, _ptr(beams), _ptr(unpacker), _ptr(packed_len), W, L,
-        _ptr(out["argmax"]), _ptr(out["accept_len"]), _ptr(out["best_beam"]),
-        _ptr(out["n_accepted"]), _ptr(out["out_tokens"]), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream)))
+                                dtype=torch.uint8, device=dev)
+    elif workspace.device != dev or not workspace.is_contiguous():
+        raise ValueError(f"workspace must be a contiguous tensor on {dev}")
+    _run("rd_greedy_accept", logits,
+         _ptr(logits), B, P, V, _ptr(beams), _ptr(unpacker), _ptr(packed_len), W, L,
+         _ptr(out["argmax"]), _ptr(out["accept_len"]), _ptr(out["best_beam"]),
+         _ptr(out["n_accepted"]), _ptr(out["out_tokens"]), _ptr(workspace),
+         workspace.numel() * workspace.element_size(), _ptr(dev_status), stream=stream)
     return out
 
 
@@ -357,13 +416,13 @@ def rd_sample_accept(target_logits, draft_logits, temperature: float, beams, pac
     rd_sample_accept in rd.h).  Returns dict(accept_len, best_beam, n_accepted,
     out_tokens)."""
     _need(target_logits, "target_logits", torch.bfloat16, ndim=3)
-    _need(draft_logits, "draft_logits", torch.bfloat16, ndim=3)
-    _need(beams, "beams", torch.int32, ndim=3)
-    _need(packer, "packer", torch.int32, ndim=2)
-    _need(unpacker, "unpacker", torch.int32, ndim=3)
-    _need(packed_len, "packed_len", torch.int32, ndim=1)
-    _need(u_accept, "u_accept", torch.float32, ndim=2)
-    _need(u_sample, "u_sample", torch.float32, ndim=2)
+    _need(draft_logits, "draft_logits", torch.bfloat16, target_logits.device, ndim=3)
+    _need(beams, "beams", torch.int32, target_logits.device, ndim=3)
+    _need(packer, "packer", torch.int32, target_logits.device, ndim=2)
+    _need(unpacker, "unpacker", torch.int32, target_logits.device, ndim=3)
+    _need(packed_len, "packed_len", torch.int32, target_logits.device, ndim=1)
+    _need(u_accept, "u_accept", torch.float32, target_logits.device, ndim=2)
+    _need(u_sample, "u_sample", torch.float32, target_logits.device, ndim=2)
     B, P, V = target_logits.shape
     _, W, L = beams.shape
     if draft_logits.shape != target_logits.shape or packer.shape != (B, P):
@@ -375,11 +434,11 @@ def rd_sample_accept(target_logits, draft_logits, temperature: float, beams, pac
                    best_beam=_empty((B,), torch.int32, target_logits),
                    n_accepted=_empty((B,), torch.int32, target_logits),
                    out_tokens=_empty((B, L), torch.int32, target_logits))
-    _check("rd_sample_accept", _lib.rd_sample_accept(
+    _run("rd_sample_accept", target_logits,
         _ptr(target_logits), _ptr(draft_logits), B, P, V, float(temperature), _ptr(beams),
         _ptr(packer), _ptr(unpacker), _ptr(packed_len), W, L, _ptr(u_accept), _ptr(u_sample),
         _ptr(out["accept_len"]), _ptr(out["best_beam"]), _ptr(out["n_accepted"]),
-        _ptr(out["out_tokens"]), _ptr(dev_status), _stream(stream)))
+        _ptr(out["out_tokens"]), _ptr(dev_status), stream=stream)
     return out
 
 
@@ -387,24 +446,23 @@ def rd_greedy_accept_noalloc(logits, beams, unpacker, packed_len, *, out=None, d
                              stream=None) -> dict:
     """rd_greedy_accept without a caller workspace, for callers that cannot allocate
     device memory: the scratch is a fixed array inside librd shared by every call
-    on the device, so calls must not overlap on the GPU.  Limits: B * P_max <= 65536.
-    (The outputs are allocated here only when `out` is not given.)"""
+    on the device, so calls must not overlap on the GPU.  Limits: B * P_max <= 65536
+    and B <= 65535.  (The outputs are allocated here only when `out` is not given:
+    a caller that cannot allocate passes them.)"""
+    shapes = _accept_shapes(logits, beams, unpacker, packed_len, out)
+    dev = logits.device
     _need(logits, "logits", torch.bfloat16, ndim=3)
-    _need(beams, "beams", torch.int32, ndim=3)
-    _need(unpacker, "unpacker", torch.int32, ndim=3)
-    _need(packed_len, "packed_len", torch.int32, ndim=1)
+    _need(beams, "beams", torch.int32, dev, ndim=3)
+    _need(unpacker, "unpacker", torch.int32, dev, ndim=3)
+    _need(packed_len, "packed_len", torch.int32, dev, ndim=1)
     B, P, V = logits.shape
     _, W, L = beams.shape
     if out is None:
-        out = dict(argmax=_empty((B, P), torch.int32, logits),
-                   accept_len=_empty((B, W), torch.int32, logits),
-                   best_beam=_empty((B,), torch.int32, logits),
-                   n_accepted=_empty((B,), torch.int32, logits),
-                   out_tokens=_empty((B, L), torch.int32, logits))
-    _check("rd_greedy_accept_noalloc", _lib.rd_greedy_accept_noalloc(
-        _ptr(logits), B, P, V, _ptr(beams), _ptr(unpacker), _ptr(packed_len), W, L,
-        _ptr(out["argmax"]), _ptr(out["accept_len"]), _ptr(out["best_beam"]),
-        _ptr(out["n_accepted"]), _ptr(out["out_tokens"]), _ptr(dev_status), _stream(stream)))
+        out = {k: _empty(shapes[k], torch.int32, logits) for k in _ACCEPT_OUTS}
+    _run("rd_greedy_accept_noalloc", logits,
+         _ptr(logits), B, P, V, _ptr(beams), _ptr(unpacker), _ptr(packed_len), W, L,
+         _ptr(out["argmax"]), _ptr(out["accept_len"]), _ptr(out["best_beam"]),
+         _ptr(out["n_accepted"]), _ptr(out["out_tokens"]), _ptr(dev_status), stream=stream)
     return out
 
 
@@ -414,16 +472,24 @@ def rd_beam_search_step(logits, scores_in, beams_in, *, out=None, dev_status=Non
     logits bf16 [B, W, V], scores_in fp32 [B, W], beams_in int32 [B, W, t].
     Returns dict(beams [B, W, t+1], scores [B, W], parent [B, W])."""
     _need(logits, "logits", torch.bfloat16, ndim=3)
-    _need(scores_in, "scores_in", torch.float32, ndim=2)
-    _need(beams_in, "beams_in", torch.int32, ndim=3)
+    _need(scores_in, "scores_in", torch.float32, logits.device, ndim=2)
+    _need(beams_in, "beams_in", torch.int32, logits.device, ndim=3)
     B, W, V = logits.shape
     t = beams_in.shape[2]
     if out is None:
         out = dict(beams=_empty((B, W, t + 1), torch.int32, logits),
                    scores=_empty((B, W), torch.float32, logits),
                    parent=_empty((B, W), torch.int32, logits))
-    _check("rd_beam_search_step", _lib.rd_beam_search_step(
+    _run("rd_beam_search_step", logits,
         _ptr(logits), _ptr(scores_in), _ptr(beams_in) if t > 0 else None, B, W, V, t,
         _ptr(out["beams"]), _ptr(out["scores"]), _ptr(out["parent"]), _ptr(dev_status),
-        _stream(stream)))
+        stream=stream)
     return out
+
+
+def rd_debug_stall_attention(budget_cycles: int) -> None:
+    """Failure-detection test hook (see rd_debug_stall_attention in rd.h): with
+    budget_cycles > 0, every later attention launch first waits, for at most that
+    many SM clock cycles, on a barrier that nothing completes, so its bounded
+    wait runs out and the kernel reports DEV_TIMEOUT and returns.  0 disarms it."""
+    _lib.rd_debug_stall_attention(int(budget_cycles))

@@ -114,6 +114,9 @@ struct TcArgs {
     const uint16_t* k_new;
     const uint16_t* v_new;
     float k_inv, v_inv, out_scale;
+    // failure-detection test hook: > 0 makes the MMA issuer first wait, with
+    // this clock budget, on a barrier that nothing completes
+    long long stall_budget;
 };
 
 struct Barriers {
@@ -128,6 +131,8 @@ struct Barriers {
     uint64_t drain;
     uint64_t f8_full[4];
     uint64_t f8_empty[4];
+    uint64_t grp;            // softmax warps' group sync in the split epilogue
+    uint64_t never;          // completed by nobody (failure-detection test hook)
     uint32_t tmem_base;
     int abort;
 };
@@ -356,6 +361,8 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
         mbar_init(&bar.drain, F8 ? 1 : 2);
         mbar_init(&bar.p_free[0], 1);
         mbar_init(&bar.p_free[1], 1);
+        mbar_init(&bar.grp, kSoftmaxThreads / 32);
+        mbar_init(&bar.never, 1);
         bar.abort = 0;
         mbar_fence_init();
     }
@@ -566,6 +573,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             const uint64_t k_desc = smem_desc(smem_addr(smem + C::kStageOff), 16, 1024, kSwizzle128B);
             const uint64_t v_desc = smem_desc(smem_addr(smem + C::kStageOff + C::kKBytes), C::kNc * 128,
                                               1024, kSwizzle128B);
+            if (a.stall_budget > 0 && !mbar_wait(&bar.never, 0, abort, a.stall_budget)) fail();
             for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
                 const UnitGeo geo = unit_geo<C::kNc>(a, u);
                 if (!geo.live) continue;
@@ -689,6 +697,12 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar.q_full);
+        };
+        uint32_t grp_uses = 0;
+        auto group_sync = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.grp);
+            return warp_wait(&bar.grp, (grp_uses++) & 1, abort, kWaitBudget);
         };
         uint32_t g = 0, unit_iter = 0;
         int q_unit = -1;                                   // unit whose queries are already written
@@ -959,12 +973,14 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 }
                 if (hf == 0) a.ml_part[prow * a.splits + geo.split] = make_float2(m, l_row);
                 __threadfence();
-                asm volatile("bar.sync 1, %0;" ::"r"(kSoftmaxThreads));
+                // The four softmax warps meet on an mbarrier (a bounded wait, unlike a
+                // named barrier: a warp that gave up elsewhere cannot strand the others)
+                if (!group_sync()) { fail(); break; }
                 if (tid == 0) {
                     const unsigned tk = atomicAdd(a.tickets + unit_id, 1u);
                     s_last = (tk == (unsigned)geo.n_splits - 1u);
                 }
-                asm volatile("bar.sync 1, %0;" ::"r"(kSoftmaxThreads));
+                if (!group_sync()) { fail(); break; }
                 if (s_last) {
                     __threadfence();
                     // paired: lane half 1 writes the zero rows 64-127 of the tile
@@ -1024,7 +1040,7 @@ bool make_kv_map(CUtensorMap* map, const void* base, int64_t rows, int heads, in
     return r == CUDA_SUCCESS;
 }
 
-// [rows, heads, D] e4m3 -> boxes of 128 positions x 1 head x D bytes, 128-byte swizzle
+// [rows, heads, D] e4m3 -> boxes of kNc (64) positions x 1 head x D bytes, 128-byte swizzle
 bool make_fp8_map(CUtensorMap* map, const void* base, int64_t rows, int heads, int D)
 {
     auto fn = encode_fn();
@@ -1040,18 +1056,6 @@ bool make_fp8_map(CUtensorMap* map, const void* base, int64_t rows, int heads, i
     return r == CUDA_SUCCESS;
 }
 
-int num_sms()
-{
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0) n = 148;
-    }
-    return n;
-}
-
 }  // namespace
 
 rd_attn_plan rd_attn_make_plan(bool causal, int B, int P_max, int Hq, int Hkv, int D,
@@ -1065,7 +1069,7 @@ rd_attn_plan rd_attn_make_plan(bool causal, int B, int P_max, int Hq, int Hkv, i
     if (plan.tiles < 1) plan.tiles = 1;
     const long ctx_chunks = causal ? 1 : ((long)max_kv + kN - 1) / kN;
     const long base_units = (long)B * Hkv * plan.tiles;
-    const long target = 3L * 152;                         // split units wanted (GB300: 152 SMs)
+    const long target = 3L * rd_device_sm_count();        // split units wanted: 3 per SM
     long cps = ctx_chunks > 0 ? ctx_chunks : 1;           // context chunks per split
     if (!causal && base_units < target && ctx_chunks > 4) {
         long want = (target + base_units - 1) / base_units;
@@ -1148,7 +1152,8 @@ cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, in
     const void* kd = causal ? k_new : k_new;
     const void* vd = causal ? v_new : v_new;
     if (kc == nullptr || kc_rows == 0) { kc = kd; vc = vd; }
-    const int grid = (int)std::min<long>((long)a.n_units, (long)num_sms());
+    const int grid = (int)std::min<long>((long)a.n_units, (long)rd_device_sm_count());
+    a.stall_budget = rd_attention_stall_budget();
     if (fp8 != nullptr) {
         // 8-bit context maps (the drafts are read by the converter warps)
         if (D != 128 || causal || paged || total_kv < 1 ||

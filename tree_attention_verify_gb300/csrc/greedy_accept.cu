@@ -211,7 +211,7 @@ rd_accept_plan rd_accept_make_plan(int B, int P_max, int V)
 {
     // enough CTAs to cover the SMs several times, but at least ~16 KB per CTA
     const long rows = (long)B * P_max;
-    const long target_ctas = 8L * 152;
+    const long target_ctas = 8L * rd_device_sm_count();
     long splits = (target_ctas + rows - 1) / rows;
     long max_splits = ((long)V * 2 + 16383) / 16384;
     if (splits > max_splits) splits = max_splits;

@@ -11,7 +11,7 @@
 //
 // Limits and sharing:
 //  - the array holds kMaxRows argmax keys and kMaxRequests tickets
-//    (B * P_max <= kMaxRows and B <= kMaxRequests, else RD_ERR_UNSUPPORTED);
+//    (B * P_max <= 65536 and B <= 65535, else RD_ERR_UNSUPPORTED);
 //    every GPU that loads librd holds it (about 768 KB) until the process exits;
 //  - every call on a device uses the same array: calls whose kernels overlap on
 //    the GPU (two streams, or two threads) race and give wrong results;
@@ -19,7 +19,8 @@
 //    before its kernel, so a previous call's leftovers never leak into it;
 //  - the first call on a device looks up the array's device address
 //    (cudaGetSymbolAddress) with that device current; make that first call
-//    before any stream capture begins.
+//    before any stream capture begins.  The address is cached for the life of
+//    the process, so it is stale after a cudaDeviceReset of that device.
 #include <mutex>
 
 #include "rd_internal.cuh"
@@ -27,7 +28,7 @@
 namespace {
 
 constexpr size_t kMaxRows = 65536;         // B * P_max
-constexpr size_t kMaxRequests = 65536;     // B
+constexpr size_t kMaxRequests = 65535;     // B
 constexpr size_t kKeyBytes = kMaxRows * sizeof(unsigned long long);
 constexpr size_t kScratchBytes = kKeyBytes + kMaxRequests * sizeof(unsigned int);
 

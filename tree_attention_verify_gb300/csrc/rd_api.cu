@@ -1,8 +1,14 @@
 // C entry points of librd: host-side validation, then one launch per call on the
 // caller's stream.  See include/rd.h for the contract of every function.
+#include <atomic>
+
 #include "rd_internal.cuh"
 
 namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<long long> g_stall_budget{0};
 
 rd_status from_cuda(cudaError_t e) { return e == cudaSuccess ? RD_OK : RD_ERR_CUDA; }
 
@@ -16,7 +22,38 @@ bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr
 
 }  // namespace
 
+int rd_device_sm_count()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+        cudaGetLastError();                       // do not leave the error for a later call
+        return kRdFallbackSms;
+    }
+    if (dev >= kMaxDevices) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            return kRdFallbackSms;
+        return n;
+    }
+    int n = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (n <= 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            return kRdFallbackSms;
+        }
+        g_sm_count[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
+long long rd_attention_stall_budget() { return g_stall_budget.load(std::memory_order_relaxed); }
+
 extern "C" {
+
+void rd_debug_stall_attention(long long budget_cycles)
+{
+    g_stall_budget.store(budget_cycles > 0 ? budget_cycles : 0, std::memory_order_relaxed);
+}
 
 const char* rd_status_string(rd_status s)
 {

@@ -14,6 +14,15 @@ __device__ __forceinline__ void rd_flag(int32_t* status, unsigned bits)
     if (status != nullptr) atomicOr(reinterpret_cast<int*>(status), static_cast<int>(bits));
 }
 
+// Number of SMs of the current device (looked up once per device); the grid
+// and split plans are sized from it.  Without a visible device (a host-only
+// workspace query) it returns kRdFallbackSms, the count of a GB300.
+constexpr int kRdFallbackSms = 152;
+int rd_device_sm_count();
+
+// Clock budget of the planted wait armed by rd_debug_stall_attention (0 = off).
+long long rd_attention_stall_budget();
+
 // Launchers (one per kernel family), called by the C entry points in rd_api.cu
 // after host-side validation.  Each returns the cudaGetLastError() of its launches.
 cudaError_t rd_launch_pack(const int32_t* beams, int B, int W, int L, int P_cap,

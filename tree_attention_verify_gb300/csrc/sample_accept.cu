@@ -450,8 +450,9 @@ int rd_sample_cluster_size(int B)
     // enough CTAs to cover the SMs once, at most kMaxCluster per request (a
     // sweep at B = 64 / 16 / 1 found 4 / 8 / 4-8 CTAs per request fastest:
     // more CTAs add cluster-barrier cost to every pass, fewer add pass length)
+    const long sms = rd_device_sm_count();
     int c = 1;
-    while (c < kMaxCluster && (long)B * c < 152) c *= 2;
+    while (c < kMaxCluster && (long)B * c < sms) c *= 2;
     return c;
 }
 

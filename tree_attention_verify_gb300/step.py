@@ -35,7 +35,7 @@ class VerifyStep:
                         best_beam=torch.empty(B, **i32), n_accepted=torch.empty(B, **i32),
                         out_tokens=torch.empty(B, L, **i32))
         self.hidden_out = torch.empty(B, W, L, Dh, dtype=torch.bfloat16, device=dev)
-        ws_a = rd_tree_attention_workspace_size(B, P, Hq, Hkv, D, max_ctx)
+        ws_a = rd_tree_attention_workspace_size(B, P, Hq, Hkv, D, max_ctx, dev)
         self.ws_attn = torch.zeros(ws_a, dtype=torch.uint8, device=dev) if ws_a else None
         self.ws_acc = torch.zeros(max(8, rd_greedy_accept_workspace_size(B, P, V)),
                                   dtype=torch.uint8, device=dev)
