@@ -51,13 +51,24 @@ using namespace rdtc;
 
 constexpr int kM = 128;                    // query rows per tile = TMEM lanes
 constexpr int kN = 64;                     // KV positions per chunk
-constexpr int kSoftmaxThreads = 128;
-constexpr int kThreads = kSoftmaxThreads + 96;          // + producer, S issuer, PV issuer
-constexpr int kThreadsF8 = kSoftmaxThreads + 64 + 128;  // + producer, MMA issuer, 4 converters
+constexpr int kCtasPerSm = 2;              // two independent pipelines per SM
+constexpr int kSoftmaxWarps = 4;           // warpgroup 0
+constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
+// Warpgroup 1: producer, MMA issuer (S and PV), two FP8 converter warps (idle in bf16).
+constexpr int kThreads = kSoftmaxThreads + 128;
 constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;                // S issuer (FP8: S and PV) and TMEM owner
-constexpr int kPvWarp = 6;                 // bf16 only: PV issuer
-constexpr int kConvWarp0 = 6;              // FP8 only: first converter warp
+constexpr int kMmaWarp = 5;                // S and PV issuer and TMEM owner
+constexpr int kConvWarp0 = 6;              // FP8 only: converter warps 6 and 7
+// Register split (setmaxnreg): two CTAs of 256 threads share an SM, so each CTA
+// launches with 128 registers per thread, 32,768 in all; warpgroup 1 gives back
+// down to kRegsOther and the softmax warpgroup takes kRegsSoftmax:
+// 128 x (192 + 64) = 32,768, and two CTAs' (192 + 64) registers x 32 lanes fit
+// one SM sub-partition's 16,384.
+constexpr int kRegsLaunch = 128;
+constexpr int kRegsSoftmax = 192;
+constexpr int kRegsOther = 64;
+static_assert(128 * (kRegsSoftmax + kRegsOther) <= kThreads * kRegsLaunch, "register split");
+static_assert(32 * kCtasPerSm * (kRegsSoftmax + kRegsOther) <= 16384, "register split per sub-partition");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when a max grows by > 2^8
 constexpr long long kWaitBudget = 4000000000LL;   // ~2 s of SM clock per wait
@@ -65,9 +76,9 @@ constexpr long long kWaitBudget = 4000000000LL;   // ~2 s of SM clock per wait
 template <int D, bool F8 = false> struct Cfg {
     static constexpr int kNc = kN;                      // KV positions per chunk
     static constexpr int kDB = D / 64;                  // 64-element (128-byte) column blocks
-    // 16-bit ring and (FP8) 8-bit ring of context chunks, 224 KB in all
-    static constexpr int kStages = F8 ? 5 : (D == 128 ? 7 : 8);
-    static constexpr int kF8Stages = F8 ? 4 : 0;
+    // 16-bit ring and (FP8) 8-bit ring of context chunks, 96 KB per CTA
+    static constexpr int kStages = F8 ? 2 : (D == 128 ? 3 : 6);
+    static constexpr int kF8Stages = F8 ? 2 : 0;
     static constexpr int kF8Ring = kF8Stages > 0 ? kF8Stages : 1;   // ring index modulus
     static constexpr int kKBytes = kNc * D * 2;         // one K (or V) chunk
     static constexpr int kStageBytes = 2 * kKBytes;
@@ -76,17 +87,15 @@ template <int D, bool F8 = false> struct Cfg {
     static constexpr int kF8Off = kStageOff + kStages * kStageBytes;
     static constexpr int kBarOff = kF8Off + kF8Stages * kF8Bytes;
     static constexpr int kSmemBytes = kBarOff + 512 + 1024;   // + barriers + alignment slack
-    // Tensor memory (32-bit columns x 128 lanes): S double buffer, O
-    // accumulator, and as 16-bit pairs (the A operands of the two MMAs) the P
-    // double buffer and two Q buffers, one per unit parity, so that the next
-    // unit's queries can be written while the current unit drains.
-    static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t kSCol = 0;                // 2 x kNc
-    static constexpr uint32_t kOCol = 2 * kNc;          // D (<= 128)
-    static constexpr uint32_t kQCol = kOCol + 128;      // D / 2, unit parity 0
-    static constexpr uint32_t kPCol = kQCol + 64;       // 2 x kNc / 2
-    static constexpr uint32_t kPStride = kNc / 2;       // columns between P buffers
-    static constexpr uint32_t kQStride = 128;           // Q of unit parity 1 at kQCol + 128
+    // Tensor memory (32-bit columns x 128 lanes), a quarter of the SM's per CTA:
+    // the S tile, with P (16-bit pairs, the A operand of PV) written over its
+    // first half once S is in registers; the O accumulator; the tile's queries
+    // (16-bit pairs, the A operand of S).
+    static constexpr uint32_t kTmemCols = 256;
+    static constexpr uint32_t kSCol = 0;                // kNc columns; P in [0, kNc / 2)
+    static constexpr uint32_t kOCol = kNc;              // D (<= 128) columns
+    static constexpr uint32_t kQCol = kOCol + 128;      // D / 2 (<= 64) columns
+    static_assert(kQCol + 64 <= kTmemCols, "tensor memory layout");
 };
 
 struct TcArgs {
@@ -122,12 +131,12 @@ struct TcArgs {
 struct Barriers {
     uint64_t kv_full[8];
     uint64_t kv_empty[8];
-    uint64_t s_full[2];
-    uint64_t s_free[2];
-    uint64_t p_full[2];
-    uint64_t p_free[2];
-    uint64_t o_final;
-    uint64_t q_full;
+    uint64_t s_full;         // S of the current chunk is in tensor memory
+    uint64_t p_full;         // P of the current chunk is written (softmax warps)
+    uint64_t o_final;        // PV of the unit's last chunk has completed
+    uint64_t o_free;         // the epilogue has read O (softmax warps)
+    uint64_t q_full;         // the unit's queries are written (softmax warps)
+    uint64_t q_free;         // every S MMA of the unit has completed
     uint64_t drain;
     uint64_t f8_full[4];
     uint64_t f8_empty[4];
@@ -135,7 +144,9 @@ struct Barriers {
     uint64_t never;          // completed by nobody (failure-detection test hook)
     uint32_t tmem_base;
     int abort;
+    int last;                // this CTA took the last ticket of a split unit
 };
+static_assert(sizeof(Barriers) <= 512, "barrier block");
 
 // Geometry of one work unit, computed identically by every role.
 struct UnitGeo {
@@ -155,14 +166,15 @@ template <int NC>
 __device__ __forceinline__ UnitGeo unit_geo(const TcArgs& a, int u)
 {
     UnitGeo g;
-    // Units run split-major, then tile, request and kv head: the CTAs take units
-    // round-robin, and this order spreads the dead units (splits past a short
-    // context, tiles past the valid rows) and the long and short causal tiles
-    // evenly over them.
+    // Units run tile-major, then split, request and kv head: the CTAs take units
+    // round-robin, and this order puts the tiles past the valid rows of a tree
+    // batch (mostly padding) last instead of interleaving them with the live
+    // units, while the splits of one tile level and the long and short causal
+    // tiles still spread evenly over the CTAs.
     const int bh = a.B * a.Hkv;
-    g.split = u / (a.tiles * bh);
-    const int rem = u % (a.tiles * bh);
-    g.tile = rem / bh;
+    g.tile = u / (a.splits * bh);
+    const int rem = u % (a.splits * bh);
+    g.split = rem / bh;
     g.b = (rem % bh) / a.Hkv;
     g.h = rem % a.Hkv;
     g.live = false;
@@ -220,6 +232,24 @@ __device__ __forceinline__ UnitGeo unit_geo(const TcArgs& a, int u)
     return g;
 }
 
+// Prefetch into L1 the per-request words that unit_geo will read for unit u, so
+// that computing that unit's geometry later costs an L1 hit.
+__device__ __forceinline__ void prefetch_geo(const TcArgs& a, int u)
+{
+    const int b = (u % (a.B * a.Hkv)) / a.Hkv;
+    const void* p0;
+    const void* p1;
+    if (a.causal) {
+        p0 = a.lens + b;
+        p1 = a.lens + b + 1;
+    } else {
+        p0 = a.lens + b;
+        p1 = a.block_table != nullptr ? (const void*)(a.ctx_lens + b) : (const void*)(a.ctx_offsets + b);
+    }
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p0));
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p1));
+}
+
 // 16-byte chunk c of row r in a [rows][128 B] tile with the 128-byte swizzle
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
 
@@ -273,57 +303,64 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 // Combine the split partials of one output row:
-// out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s, 64 columns at a time with
-// the 16 loads of a split's part in flight together.  Kept out of line: it runs
-// once per row and unit, and inlining it into the kernel body slowed the
-// streaming loop of the single-split case.
+// out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.  The (m, l) of eight splits
+// are loaded together, and a split's (m, l) with the partial loads of half a row,
+// so a merge costs about one round trip per split and half row.  Kept out of
+// line: it runs once per row and unit, and inlining it into the kernel body
+// slowed the streaming loop of the single-split case.
 template <int D>
 __device__ __noinline__ void merge_split_row(const TcArgs& a, size_t prow, int n_splits,
                                              bool valid, uint16_t* dst)
 {
+    constexpr int NC = D / 2;                           // columns per pass
     const float2* mlp = a.ml_part + prow * a.splits;
-    const float* opp = a.o_part + prow * a.splits * D;
     float M = -INFINITY;
-    for (int sp = 0; sp < n_splits; ++sp) M = fmaxf(M, __ldcg(&mlp[sp].x));
+    for (int s0 = 0; valid && s0 < n_splits; s0 += 8) {
+        float x[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = s0 + i < n_splits ? __ldcg(&mlp[s0 + i].x) : -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) M = fmaxf(M, x[i]);
+    }
     const bool any = valid && M != -INFINITY;
-    float Ls = 0.f, inv = 0.f;
+    float Ls = 0.f;
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+        const float* opp = a.o_part + prow * a.splits * D + half * NC;
+        float acc[NC];
 #pragma unroll
-    for (int h = 0; h < D / 64; ++h) {
-        float acc[64];
-#pragma unroll
-        for (int c = 0; c < 64; ++c) acc[c] = 0.f;
+        for (int c = 0; c < NC; ++c) acc[c] = 0.f;
         for (int sp = 0; any && sp < n_splits; ++sp) {
             const float2 ml = __ldcg(&mlp[sp]);
-            if (ml.x == -INFINITY) continue;
-            const float w = exp2f(ml.x - M);
-            if (h == 0) Ls += ml.y * w;
-            const float4* src = reinterpret_cast<const float4*>(opp + (size_t)sp * D + h * 64);
-            float4 x[16];
+            const float4* src = reinterpret_cast<const float4*>(opp + (size_t)sp * D);
+            float4 x[NC / 4];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) x[i] = __ldcg(src + i);
+            for (int i = 0; i < NC / 4; ++i) x[i] = __ldcg(src + i);
+            const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+            if (half == 0) Ls += ml.y * w;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < NC / 4; ++i) {
                 acc[4 * i + 0] += x[i].x * w;
                 acc[4 * i + 1] += x[i].y * w;
                 acc[4 * i + 2] += x[i].z * w;
                 acc[4 * i + 3] += x[i].w * w;
             }
         }
-        if (h == 0) inv = (any && Ls > 0.f) ? a.out_scale / Ls : 0.f;
+        const float inv = (any && Ls > 0.f) ? a.out_scale / Ls : 0.f;
 #pragma unroll
-        for (int c = 0; c < 64; c += 8) {
+        for (int c = 0; c < NC; c += 8) {
             uint4 v;
             v.x = pack_bf16(acc[c + 0] * inv, acc[c + 1] * inv);
             v.y = pack_bf16(acc[c + 2] * inv, acc[c + 3] * inv);
             v.z = pack_bf16(acc[c + 4] * inv, acc[c + 5] * inv);
             v.w = pack_bf16(acc[c + 6] * inv, acc[c + 7] * inv);
-            *reinterpret_cast<uint4*>(dst + h * 64 + c) = v;
+            *reinterpret_cast<uint4*>(dst + half * NC + c) = v;
         }
     }
 }
 
 template <int D, bool F8>
-__global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
 tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map_kc,
                          const __grid_constant__ CUtensorMap map_vc,
                          const __grid_constant__ CUtensorMap map_kd,
@@ -334,7 +371,6 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Barriers& bar = *reinterpret_cast<Barriers*>(smem + C::kBarOff);
-    __shared__ int s_last;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -343,25 +379,21 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
 
     if (tid == 0) {
         for (int i = 0; i < C::kStages; ++i) {
-            // FP8: the four converter warps (two write K, two V)
-            mbar_init(&bar.kv_full[i], F8 ? 4 : 1);
+            mbar_init(&bar.kv_full[i], F8 ? 2 : 1);        // FP8: the two converter warps
             mbar_init(&bar.kv_empty[i], 1);                // PV (after S) has read the stage
         }
         for (int i = 0; i < C::kF8Stages; ++i) {
             mbar_init(&bar.f8_full[i], 1);
-            mbar_init(&bar.f8_empty[i], 4);
+            mbar_init(&bar.f8_empty[i], 2);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&bar.s_full[i], 1);
-            mbar_init(&bar.s_free[i], 4);
-            mbar_init(&bar.p_full[i], 4);
-        }
+        mbar_init(&bar.s_full, 1);
+        mbar_init(&bar.p_full, kSoftmaxWarps);
         mbar_init(&bar.o_final, 1);
-        mbar_init(&bar.q_full, 4);
-        mbar_init(&bar.drain, F8 ? 1 : 2);
-        mbar_init(&bar.p_free[0], 1);
-        mbar_init(&bar.p_free[1], 1);
-        mbar_init(&bar.grp, kSoftmaxThreads / 32);
+        mbar_init(&bar.o_free, kSoftmaxWarps);
+        mbar_init(&bar.q_full, kSoftmaxWarps);
+        mbar_init(&bar.q_free, 1);
+        mbar_init(&bar.drain, 1);
+        mbar_init(&bar.grp, kSoftmaxWarps);
         mbar_init(&bar.never, 1);
         bar.abort = 0;
         mbar_fence_init();
@@ -385,21 +417,11 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
         *abort = 1;
         rd_flag(a.status, RD_DEV_TIMEOUT);
     };
-    // O += P V for chunk gp (K-steps of 16 positions; A = P in TMEM, B = the V
-    // stage); the commits release the stage (S of the chunk completed before
-    // its P was written) and the P buffer.
-    auto issue_pv = [&](uint32_t gp, bool first, uint64_t v_desc) {
-        constexpr uint32_t idPV = F8 ? idesc_f16(kM, D, false, true) : idesc_bf16(kM, D, false, true);
-        const uint64_t vd = v_desc + (uint64_t)(((gp % C::kStages) * C::kStageBytes) >> 4);
-        const uint32_t pt = tmem + C::kPCol + (gp & 1) * C::kPStride;
-#pragma unroll
-        for (int kk = 0; kk < C::kNc / 16; ++kk)
-            mma_tmem_a(tmem + C::kOCol, pt + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), idPV,
-                       !(first && kk == 0));
-        mma_commit(&bar.kv_empty[gp % C::kStages]);
-        mma_commit(&bar.p_free[gp & 1]);
-    };
 
+    if (warp >= kSoftmaxWarps) {
+    // Warpgroup 1 gives registers back first (all four warps, unconditionally),
+    // then splits into its roles.
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
     if (F8 && warp == kProducerWarp) {
         // ------------------------------------------------- producer (8-bit context)
         if (lane == 0) {
@@ -429,11 +451,9 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
         }
     } else if (F8 && warp >= kConvWarp0) {
         // ------------------------------------------------------------ converters
-        // Threads 0-63 write the K rows of a 16-bit stage, threads 64-127 its V
-        // rows; the stage is released as one once PV has read it.
-        const int ct = tid - kConvWarp0 * 32;
-        const int row = ct & 63;
-        const bool do_k = ct < 64;                 // warp-uniform
+        // Thread row (0-63) writes K row `row` and V row `row` of a 16-bit stage;
+        // the stage is released as one once PV has read it.
+        const int row = tid - kConvWarp0 * 32;
         uint32_t g = 0, g8 = 0;
         // one 128-byte e4m3 row (swizzled) -> one 256-byte f16 row in two 128-byte blocks
         auto widen_row = [&](const unsigned char* src, unsigned char* dst) {
@@ -490,12 +510,12 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                     break;
                 }
                 const int d = (j - geo.n_ctx) * C::kNc + row;       // draft row (drafts only)
-                if (do_k) {
-                    if (ctx) widen_row(src, kdst);
-                    else draft_row(a.k_new, geo, d, a.k_inv, kdst);
+                if (ctx) {
+                    widen_row(src, kdst);
+                    widen_row(src + C::kNc * D, vdst);
                 } else {
-                    if (ctx) widen_row(src + C::kNc * D, vdst);
-                    else draft_row(a.v_new, geo, d, a.v_inv, vdst);
+                    draft_row(a.k_new, geo, d, a.k_inv, kdst);
+                    draft_row(a.v_new, geo, d, a.v_inv, vdst);
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -559,13 +579,18 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 mbar_wait(&bar.kv_full[k % C::kStages], (k / C::kStages) & 1, &no_abort, kWaitBudget);
         }
     } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------- S issuer
-        // S = Q K^T for every chunk as soon as it has landed and its TMEM tile is
-        // free.  bf16: PV runs from its own warp, so the two chains overlap.
-        // FP8: this thread also issues PV_{j-1} right after S_j, once the
-        // softmax has written P_{j-1} (measured faster there than a PV warp).
+        // ------------------------------------------------------- MMA issuer
+        // Per chunk: S = Q K^T into the S/P columns once the chunk has landed,
+        // right behind PV of the chunk before (whose A operand, P, lives in those
+        // columns: the MMAs of one thread run in issue order, so S writes them
+        // after PV has read them, and the commit behind S also tracks that PV);
+        // then, once the softmax warps have written P over S, O += P V.  After
+        // the last S of a unit, q_free tells the softmax warps that the queries
+        // may be overwritten; before the first PV of a unit (which restarts O),
+        // o_free that the epilogue of the unit before has read O.
         if (lane == 0) {
             constexpr uint32_t idS = F8 ? idesc_f16(kM, C::kNc, false, false) : idesc_bf16(kM, C::kNc, false, false);
+            constexpr uint32_t idPV = F8 ? idesc_f16(kM, D, false, true) : idesc_bf16(kM, D, false, true);
             uint32_t g = 0, unit_iter = 0;
             // Shared-memory descriptors differ only in their start-address field
             // (bits 0-13, address >> 4): build the base once and add offsets,
@@ -579,46 +604,41 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 if (!geo.live) continue;
                 const int n = geo.n_ctx + geo.n_draft;
                 if (!mbar_wait(&bar.q_full, unit_iter & 1, abort, kWaitBudget)) { fail(); break; }
-                tc_fence_after();
                 bool ok = true;
                 for (int j = 0; j < n; ++j) {
                     const uint32_t gg = g + j;
-                    if (!mbar_wait(&bar.kv_full[gg % C::kStages], (gg / C::kStages) & 1, abort, kWaitBudget) ||
-                        (gg >= 2 && !mbar_wait(&bar.s_free[gg & 1], ((gg >> 1) - 1) & 1, abort, kWaitBudget))) {
+                    const int st = (int)(gg % C::kStages);
+                    if (!mbar_wait(&bar.kv_full[st], (gg / C::kStages) & 1, abort, kWaitBudget)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    // D/16 K-steps into TMEM tile gg & 1
-                    const uint64_t kd = k_desc + (uint64_t)(((gg % C::kStages) * C::kStageBytes) >> 4);
-                    const uint32_t d_tmem = tmem + C::kSCol + (gg & 1) * C::kNc;
+                    // D/16 K-steps into the S columns
+                    const uint64_t kd = k_desc + (uint64_t)((st * C::kStageBytes) >> 4);
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks) {
                         const uint32_t off = ((ks >> 2) * (C::kNc * 128) + (ks & 3) * 32) >> 4;
-                        mma_tmem_a(d_tmem, tmem + C::kQCol + (unit_iter & 1) * C::kQStride + ks * 8,
-                                   kd + off, idS, ks > 0);
+                        mma_tmem_a(tmem + C::kSCol, tmem + C::kQCol + ks * 8, kd + off, idS, ks > 0);
                     }
-                    mma_commit(&bar.s_full[gg & 1]);
-                    if (F8 && j >= 1) {
-                        if (!mbar_wait(&bar.p_full[(gg - 1) & 1], ((gg - 1) >> 1) & 1, abort, kWaitBudget)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        issue_pv(gg - 1, j == 1, v_desc);
-                    }
-                }
-                if (F8 && ok) {
-                    const uint32_t gl = g + n - 1;
-                    if (!mbar_wait(&bar.p_full[gl & 1], (gl >> 1) & 1, abort, kWaitBudget)) {
+                    mma_commit(&bar.s_full);
+                    if (j == n - 1) mma_commit(&bar.q_free);
+                    if (j == 0 && unit_iter > 0 &&
+                        !mbar_wait(&bar.o_free, (unit_iter - 1) & 1, abort, kWaitBudget)) {
                         ok = false;
-                    } else {
-                        tc_fence_after();
-                        issue_pv(gl, n == 1, v_desc);
+                        break;
                     }
+                    if (!mbar_wait(&bar.p_full, gg & 1, abort, kWaitBudget)) { ok = false; break; }
+                    tc_fence_after();
+                    // O += P V: K-steps of 16 positions, A = P over the S columns
+                    const uint64_t vd = v_desc + (uint64_t)((st * C::kStageBytes) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < C::kNc / 16; ++kk)
+                        mma_tmem_a(tmem + C::kOCol, tmem + C::kSCol + kk * 8,
+                                   vd + (uint64_t)((kk * 2048) >> 4), idPV, j > 0 || kk > 0);
+                    mma_commit(&bar.kv_empty[st]);
                 }
                 if (!ok) { fail(); break; }
-                if (F8) mma_commit(&bar.o_final);
+                mma_commit(&bar.o_final);
                 g += n;
                 ++unit_iter;
             }
@@ -626,35 +646,10 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             mma_commit(&bar.drain);
             mbar_wait(&bar.drain, 0, &no_abort, kWaitBudget);
         }
-    } else if (!F8 && warp == kPvWarp) {
-        // ------------------------------------------------------- PV issuer (bf16)
-        if (lane == 0) {
-            uint32_t g = 0;
-            const uint64_t v_desc = smem_desc(smem_addr(smem + C::kStageOff + C::kKBytes), C::kNc * 128,
-                                              1024, kSwizzle128B);
-            for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
-                const UnitGeo geo = unit_geo<C::kNc>(a, u);
-                if (!geo.live) continue;
-                const int n = geo.n_ctx + geo.n_draft;
-                bool ok = true;
-                for (int j = 0; j < n; ++j) {
-                    const uint32_t gg = g + j;
-                    if (!mbar_wait(&bar.p_full[gg & 1], (gg >> 1) & 1, abort, kWaitBudget)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    issue_pv(gg, j == 0, v_desc);
-                }
-                if (!ok) { fail(); break; }
-                mma_commit(&bar.o_final);
-                g += n;
-            }
-            mma_commit(&bar.drain);
-            mbar_wait(&bar.drain, 0, &no_abort, kWaitBudget);
-        }
+    }
     } else {
         // ------------------------------------------------------------ softmax
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
         // Thread tid owns TMEM lane tid.  A tile with more than 64 valid rows
         // keeps row r in lane r, and a thread takes all 64 columns of a chunk.
         // A tile with at most 64 valid rows is paired: row r = 16 w + (lane & 15)
@@ -663,12 +658,13 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
         // columns.  A lane's P row is zero outside its own columns, so its O is
         // the partial sum over them; the two lanes share one running maximum
         // (exchanged every chunk), so their rescales agree and their O and l add
-        // up in the epilogue.  All four warps then share the exponentials of up
-        // to 64 rows instead of two warps taking every column.
+        // up in the epilogue.
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const uint32_t s_col = tmem + lane_base + C::kSCol;
+        const uint32_t o_col = tmem + lane_base + C::kOCol;
         auto is_paired = [&](const UnitGeo& ug) { return ug.n_rows - ug.tile * kM <= 64; };
-        // the queries of unit ug -> Q buffer qb (this thread's lane, 16-bit pairs)
-        auto load_q = [&](const UnitGeo& ug, uint32_t qb) {
+        // the queries of unit ug -> the Q columns of this thread's lane
+        auto load_q = [&](const UnitGeo& ug) {
             const bool pr = is_paired(ug);
             const int qr = ug.tile * kM + (pr ? warp * 16 + (lane & 15) : tid);
             const bool qv_ok = qr < ug.n_rows;
@@ -691,7 +687,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                     qv[c * 4 + 0] = v.x; qv[c * 4 + 1] = v.y;
                     qv[c * 4 + 2] = v.z; qv[c * 4 + 3] = v.w;
                 }
-                tmem_st32(tmem + lane_base + C::kQCol + qb * C::kQStride + half * 32, qv);
+                tmem_st32(tmem + lane_base + C::kQCol + half * 32, qv);
             }
             tmem_st_wait();
             tc_fence_before();
@@ -699,7 +695,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             if (lane == 0) mbar_arrive(&bar.q_full);
         };
         uint32_t grp_uses = 0;
-        auto group_sync = [&]() -> bool {
+        auto group_sync = [&]() -> bool {              // the softmax warps, bounded
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar.grp);
             return warp_wait(&bar.grp, (grp_uses++) & 1, abort, kWaitBudget);
@@ -710,6 +706,9 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
         UnitGeo next_geo;
         for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
             const UnitGeo geo = next_u == u ? next_geo : unit_geo<C::kNc>(a, u);
+            // the words the next unit's geometry needs, into L1 now (its loads then
+            // overlap this unit's chunks)
+            if (u + (int)gridDim.x < a.n_units) prefetch_geo(a, u + gridDim.x);
             const int hq0 = geo.h * a.G;
             if (geo.zero_tile) {                           // padded rows of a tree tile
                 const int row = geo.tile * kM + tid;
@@ -730,25 +729,26 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             const int row = geo.tile * kM + r;
             const bool valid = row < geo.n_rows;
             const int qpos = row / a.G;                    // node p (tree) / token t (causal)
-            if (q_unit != u) load_q(geo, unit_iter & 1);   // not written ahead
+            // queries not written ahead (the first live unit, or one after a unit
+            // that was not live): the S MMAs of the last live unit have completed,
+            // as this warp waited for them at that unit's end
+            if (q_unit != u) load_q(geo);
             float m = -INFINITY, l = 0.f;
-            // a warp whose rows are all padding reads no scores: it keeps the
-            // barrier protocol and zeroes its P rows once per buffer and unit
+            // a warp whose rows are all padding reads no scores; it writes zero P
+            // rows (the S columns hold scores again every chunk)
             const bool dead = __all_sync(0xffffffffu, !valid);
             const uint32_t* mrow = (!a.causal && valid)
                 ? a.mask + ((size_t)geo.b * a.P_max + qpos) * a.mask_words : nullptr;
-            // One chunk: NCOL = 64 columns per lane, or 32 for a paired lane.
-            auto chunk = [&](auto ncol, uint32_t gg, int j) -> bool {
+            // One chunk: NCOL = 64 columns per lane, or 32 for a paired lane.  The
+            // commit that completed S_j also tracked PV_{j-1}, so O is stable here.
+            auto chunk = [&](auto ncol, int j) {
                 constexpr int NCOL = decltype(ncol)::value;
-                const int sb = gg & 1;
                 const int c0 = NCOL == 32 ? 32 * hf : 0;  // first column of this lane
-                const uint32_t p_col = tmem + lane_base + C::kPCol + sb * C::kPStride;
                 float s[NCOL];
                 {
                     // the load is warp-collective (one address for all lanes): read
                     // all 64 columns; a paired lane keeps its 32
                     uint32_t sr[64];
-                    const uint32_t s_col = tmem + lane_base + C::kSCol + sb * C::kNc;
                     tmem_ld32(s_col, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
                     tmem_ld32(s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
                     tmem_ld_wait();
@@ -756,9 +756,6 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                     for (int c = 0; c < NCOL; ++c)
                         s[c] = __uint_as_float(NCOL == 64 ? sr[c] : (hf ? sr[32 + c] : sr[c]));
                 }
-                tc_fence_before();                         // S is in registers: release it
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar.s_free[sb]);
                 // ---- visibility ---------------------------------------------------
                 if (!valid) {
 #pragma unroll
@@ -796,23 +793,16 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 const bool need = ms > m + kRescaleThreshold;
                 const float m_new = need ? ms : m;
                 if (__any_sync(0xffffffffu, need) && j > 0) {
-                    // O holds earlier chunks: wait until PV of the previous chunk has
-                    // completed (it then releases its P buffer; a per-buffer barrier
-                    // cannot lag two phases behind the wait), then rescale
-                    if (!warp_wait(&bar.p_free[(gg - 1) & 1], ((gg - 1) >> 1) & 1, abort, kWaitBudget))
-                        return false;
-                    tc_fence_after();
                     const float alpha = need ? fast_exp2(m - m_new) : 1.f;
 #pragma unroll
                     for (int cb = 0; cb < D / 32; ++cb) {
                         uint32_t o[32];
-                        tmem_ld32(tmem + lane_base + C::kOCol + cb * 32, o);
+                        tmem_ld32(o_col + cb * 32, o);
                         tmem_ld_wait();
 #pragma unroll
                         for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-                        tmem_st32(tmem + lane_base + C::kOCol + cb * 32, o);
+                        tmem_st32(o_col + cb * 32, o);
                     }
-                    tmem_st_wait();
                 }
                 if (need) {
                     l *= fast_exp2(m - m_new);             // 0 while m is -inf
@@ -832,70 +822,49 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
 #pragma unroll
                     for (int e = 0; e < 4; ++e) pv[c8 * 4 + e] = pack16<F8>(p[2 * e], p[2 * e + 1]);
                 }
-                // P (16-bit) into this lane's P columns, PV's A operand, once PV of
-                // the chunk two back has released that buffer; a paired lane
-                // writes zeros over the other lane's columns
-                if (gg >= 2 && !warp_wait(&bar.p_free[sb], ((gg >> 1) - 1) & 1, abort, kWaitBudget))
-                    return false;
-                tc_fence_after();
+                // P (16-bit) over the first half of this lane's S columns, PV's A
+                // operand; a paired lane writes zeros over the other lane's columns
                 if constexpr (NCOL == 64) {
-                    tmem_st32(p_col, pv);
+                    tmem_st32(s_col, pv);
                 } else {
                     uint32_t pw[32];
 #pragma unroll
                     for (int c = 0; c < 32; ++c) pw[c] = ((c >> 4) == hf) ? pv[c & 15] : 0u;
-                    tmem_st32(p_col, pw);
+                    tmem_st32(s_col, pw);
                 }
                 l += ((lsum[0] + lsum[1]) + (lsum[2] + lsum[3])) +
                      ((lsum[4] + lsum[5]) + (lsum[6] + lsum[7]));
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar.p_full[sb]);
-                return true;
             };
             bool ok = true;
             for (int j = 0; j < n; ++j) {
                 const uint32_t gg = g + j;
-                const int sb = gg & 1;
-                if (!warp_wait(&bar.s_full[sb], (gg >> 1) & 1, abort, kWaitBudget)) { ok = false; break; }
+                if (!warp_wait(&bar.s_full, gg & 1, abort, kWaitBudget)) { ok = false; break; }
                 tc_fence_after();
                 if (dead) {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bar.s_free[sb]);
-                    // like the live warps, arrive for chunk gg only once PV of chunk
-                    // gg-2 has released the buffer, so that no arrival runs ahead
-                    // into an earlier phase of p_full
-                    if (gg >= 2 && !warp_wait(&bar.p_free[sb], ((gg >> 1) - 1) & 1, abort, kWaitBudget)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    if (j < 2) {                           // zero P rows once per buffer and unit
-                        uint32_t zero[32];
+                    uint32_t zero[32];
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) zero[c] = 0u;
-                        tmem_st32(tmem + lane_base + C::kPCol + sb * C::kPStride, zero);
-                        tmem_st_wait();
-                    }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bar.p_full[sb]);
-                    continue;
+                    for (int c = 0; c < 32; ++c) zero[c] = 0u;
+                    tmem_st32(s_col, zero);
+                } else if (paired) {
+                    chunk(std::integral_constant<int, 32>{}, j);
+                } else {
+                    chunk(std::integral_constant<int, 64>{}, j);
                 }
-                ok = paired ? chunk(std::integral_constant<int, 32>{}, gg, j)
-                            : chunk(std::integral_constant<int, 64>{}, gg, j);
-                if (!ok) break;
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar.p_full);
             }
-            // the next unit's queries (if it is live) into the other Q buffer, so
-            // that its first S MMA overlaps this unit's PV drain and epilogue (the
-            // buffer's previous reader, S of the unit before this one, has
-            // completed); its geometry is kept for the next iteration
+            // every S MMA of this unit has completed once q_free does; then the next
+            // unit's queries (if it is live) go into the Q columns, so that its first
+            // S MMA overlaps this unit's PV drain and epilogue
+            if (ok && !warp_wait(&bar.q_free, unit_iter & 1, abort, kWaitBudget)) ok = false;
             if (ok && u + (int)gridDim.x < a.n_units) {
                 next_u = u + gridDim.x;
                 next_geo = unit_geo<C::kNc>(a, next_u);
                 if (next_geo.live) {
-                    load_q(next_geo, (unit_iter + 1) & 1);
+                    tc_fence_after();
+                    load_q(next_geo);
                     q_unit = next_u;
                 }
             }
@@ -906,7 +875,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             // then writes output columns [hf D/2, (hf + 1) D/2).
             const float l_row = paired ? l + __shfl_xor_sync(0xffffffffu, l, 16) : l;
             auto o_block = [&](int cb, uint32_t (&o)[32]) {
-                tmem_ld32(tmem + lane_base + C::kOCol + cb * 32, o);
+                tmem_ld32(o_col + cb * 32, o);
                 tmem_ld_wait();
                 if (paired) {
 #pragma unroll
@@ -914,6 +883,12 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                         o[c] = __float_as_uint(__uint_as_float(o[c]) +
                                                __shfl_xor_sync(0xffffffffu, __uint_as_float(o[c]), 16));
                 }
+            };
+            // O has been read: the next unit's first PV may start
+            auto release_o = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar.o_free);
             };
             auto mine = [&](int cb) { return !paired || (cb >= D / 64) == (hf == 1); };
             const bool split_mode = !a.causal && geo.n_splits > 1;
@@ -930,6 +905,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 for (int cb = 0; cb < D / 32; ++cb) {
                     uint32_t o[32];
                     o_block(cb, o);
+                    if (cb == D / 32 - 1) release_o();
                     if (write && mine(cb)) {
 #pragma unroll
                         for (int c = 0; c < 32; c += 8) {
@@ -963,6 +939,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 for (int cb = 0; cb < D / 32; ++cb) {
                     uint32_t o[32];
                     o_block(cb, o);
+                    if (cb == D / 32 - 1) release_o();
                     if (mine(cb)) {
 #pragma unroll
                         for (int c = 0; c < 32; c += 4)
@@ -973,15 +950,15 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 }
                 if (hf == 0) a.ml_part[prow * a.splits + geo.split] = make_float2(m, l_row);
                 __threadfence();
-                // The four softmax warps meet on an mbarrier (a bounded wait, unlike a
+                // The softmax warps meet on an mbarrier (a bounded wait, unlike a
                 // named barrier: a warp that gave up elsewhere cannot strand the others)
                 if (!group_sync()) { fail(); break; }
                 if (tid == 0) {
                     const unsigned tk = atomicAdd(a.tickets + unit_id, 1u);
-                    s_last = (tk == (unsigned)geo.n_splits - 1u);
+                    bar.last = (tk == (unsigned)geo.n_splits - 1u);
                 }
                 if (!group_sync()) { fail(); break; }
-                if (s_last) {
+                if (bar.last) {
                     __threadfence();
                     // paired: lane half 1 writes the zero rows 64-127 of the tile
                     const int rr = hf == 0 ? r : 64 + r;
@@ -1069,6 +1046,7 @@ rd_attn_plan rd_attn_make_plan(bool causal, int B, int P_max, int Hq, int Hkv, i
     if (plan.tiles < 1) plan.tiles = 1;
     const long ctx_chunks = causal ? 1 : ((long)max_kv + kN - 1) / kN;
     const long base_units = (long)B * Hkv * plan.tiles;
+    const long ctas = (long)kCtasPerSm * rd_device_sm_count();
     const long target = 3L * rd_device_sm_count();        // split units wanted: 3 per SM
     long cps = ctx_chunks > 0 ? ctx_chunks : 1;           // context chunks per split
     if (!causal && base_units < target && ctx_chunks > 4) {
@@ -1076,6 +1054,9 @@ rd_attn_plan rd_attn_make_plan(bool causal, int B, int P_max, int Hq, int Hkv, i
         cps = (ctx_chunks + want - 1) / want;
         if (cps < 4) cps = 4;                             // at least 256 positions per split
     }
+    // a batch with fewer than two units per CTA: no unit longer than 4096
+    // positions, so that one long context does not hold up the launch
+    if (!causal && base_units < 2 * ctas && cps > 64) cps = 64;
     plan.split_len = (int)(cps * kN);
     plan.splits = causal ? 1 : (int)((ctx_chunks + cps - 1) / cps);
     if (plan.splits < 1) plan.splits = 1;
@@ -1152,7 +1133,7 @@ cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, in
     const void* kd = causal ? k_new : k_new;
     const void* vd = causal ? v_new : v_new;
     if (kc == nullptr || kc_rows == 0) { kc = kd; vc = vd; }
-    const int grid = (int)std::min<long>((long)a.n_units, (long)rd_device_sm_count());
+    const int grid = (int)std::min<long>((long)a.n_units, (long)kCtasPerSm * rd_device_sm_count());
     a.stall_budget = rd_attention_stall_budget();
     if (fp8 != nullptr) {
         // 8-bit context maps (the drafts are read by the converter warps)
@@ -1165,7 +1146,7 @@ cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, in
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Cf::kSmemBytes);
         if (e != cudaSuccess) return e;
-        tree_attention_tc_kernel<128, true><<<grid, kThreadsF8, Cf::kSmemBytes, stream>>>(
+        tree_attention_tc_kernel<128, true><<<grid, kThreads, Cf::kSmemBytes, stream>>>(
             a, mkc, mvc, mkc, mvc);
         return cudaGetLastError();
     }
