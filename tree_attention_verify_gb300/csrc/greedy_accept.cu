@@ -23,6 +23,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kVecPerIter = 4;          // 16-byte loads in flight per thread
+constexpr int kStage = 512;             // beams / unpacker entries staged for the acceptance walk
 constexpr int kNoIndex = 0x7fffffff;
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p)
@@ -68,6 +69,77 @@ __device__ __forceinline__ void better(float& best, int& bidx, float v, int i)
     if (v > best || (v == best && i < bidx)) { best = v; bidx = i; }
 }
 
+// Acceptance of request b (the CTA that took its last ticket): decode and reset
+// the argmax keys, then walk every beam.  The request's beams and unpacker rows
+// are staged in shared memory with one coalesced load when they fit, so a beam's
+// walk costs no dependent global round trips.
+__device__ __noinline__ void accept_request(int b, int P_max, int V, int Pb, bool bad_len,
+                                            const int32_t* __restrict__ beams,
+                                            const int32_t* __restrict__ unpacker, int W, int L,
+                                            int32_t* __restrict__ argmax_out,
+                                            int32_t* __restrict__ accept_len,
+                                            int32_t* __restrict__ best_beam,
+                                            int32_t* __restrict__ n_accepted,
+                                            int32_t* __restrict__ out_tokens,
+                                            unsigned long long* keys, unsigned int* tickets,
+                                            int32_t* dev_status, int* s_g, int* s_acc,
+                                            int* s_bb, int* s_up)
+{
+    const int tid = threadIdx.x;
+    const int32_t* bb = beams + (size_t)b * W * L;
+    const int32_t* up = unpacker + (size_t)b * W * L;
+    const bool staged = W * L <= kStage;
+    for (int q = tid; q < P_max; q += kThreads) {
+        const unsigned long long k = atomicExch(keys + (size_t)b * P_max + q, 0ull);
+        const int g = (bad_len || q >= Pb) ? -1 : (int)(0xffffffffu - (uint32_t)k);
+        s_g[q] = g;
+        argmax_out[(size_t)b * P_max + q] = g;
+    }
+    if (staged) {
+        for (int i = tid; i < W * L; i += kThreads) {
+            s_bb[i] = __ldg(bb + i);
+            s_up[i] = __ldg(up + i);
+        }
+    }
+    __syncthreads();
+    const int32_t* wb = staged ? s_bb : bb;
+    const int32_t* wu = staged ? s_up : up;
+    if (tid < W) {
+        int a = 0;
+        if (!bad_len) {
+            for (int j = 1; j < L; ++j) {
+                const int prev = wu[tid * L + j - 1];
+                const int tok = wb[tid * L + j];
+                if (prev < 0 || prev >= Pb) { rd_flag(dev_status, RD_DEV_BAD_INDEX); break; }
+                if (tok < 0 || tok >= V) rd_flag(dev_status, RD_DEV_BAD_TOKEN);
+                if (tok != s_g[prev]) break;
+                a = j;
+            }
+        }
+        s_acc[tid] = a;
+        accept_len[(size_t)b * W + tid] = a;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        if (bad_len) rd_flag(dev_status, RD_DEV_BAD_LENGTH);
+        int best = 0;
+        for (int w = 1; w < W; ++w)
+            if (s_acc[w] > s_acc[best]) best = w;
+        const int a = s_acc[best];
+        best_beam[b] = best;
+        n_accepted[b] = a;
+        int32_t* ot = out_tokens + (size_t)b * L;
+        for (int j = 0; j < L; ++j) ot[j] = -1;
+        for (int j = 1; j <= a; ++j) ot[j - 1] = wb[best * L + j];
+        const int last = wu[best * L + a];
+        if (!bad_len) {
+            if (last >= 0 && last < Pb) ot[a] = s_g[last];
+            else rd_flag(dev_status, RD_DEV_BAD_INDEX);
+        }
+        tickets[b] = 0u;
+    }
+}
+
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads)
 argmax_accept_kernel(const uint16_t* __restrict__ logits, int P_max, int V, int splits,
@@ -84,6 +156,8 @@ argmax_accept_kernel(const uint16_t* __restrict__ logits, int P_max, int V, int 
     __shared__ int s_last;
     __shared__ int s_g[RD_MAX_PACKED];
     __shared__ int s_acc[RD_MAX_BEAMS];
+    __shared__ int s_bb[kStage];
+    __shared__ int s_up[kStage];
 
     const int b = blockIdx.y;
     const int p = blockIdx.x / splits;
@@ -154,50 +228,9 @@ argmax_accept_kernel(const uint16_t* __restrict__ logits, int P_max, int V, int 
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-
-    for (int q = tid; q < P_max; q += kThreads) {
-        const unsigned long long k = atomicExch(keys + (size_t)b * P_max + q, 0ull);
-        const int g = (bad_len || q >= Pb) ? -1 : (int)(0xffffffffu - (uint32_t)k);
-        s_g[q] = g;
-        argmax_out[(size_t)b * P_max + q] = g;
-    }
-    __syncthreads();
-    const int32_t* bb = beams + (size_t)b * W * L;
-    const int32_t* up = unpacker + (size_t)b * W * L;
-    if (tid < W) {
-        int a = 0;
-        if (!bad_len) {
-            for (int j = 1; j < L; ++j) {
-                const int prev = up[tid * L + j - 1];
-                const int tok = bb[tid * L + j];
-                if (prev < 0 || prev >= Pb) { rd_flag(dev_status, RD_DEV_BAD_INDEX); break; }
-                if (tok < 0 || tok >= V) rd_flag(dev_status, RD_DEV_BAD_TOKEN);
-                if (tok != s_g[prev]) break;
-                a = j;
-            }
-        }
-        s_acc[tid] = a;
-        accept_len[(size_t)b * W + tid] = a;
-    }
-    __syncthreads();
-    if (tid == 0) {
-        if (bad_len) rd_flag(dev_status, RD_DEV_BAD_LENGTH);
-        int best = 0;
-        for (int w = 1; w < W; ++w)
-            if (s_acc[w] > s_acc[best]) best = w;
-        const int a = s_acc[best];
-        best_beam[b] = best;
-        n_accepted[b] = a;
-        int32_t* ot = out_tokens + (size_t)b * L;
-        for (int j = 0; j < L; ++j) ot[j] = -1;
-        for (int j = 1; j <= a; ++j) ot[j - 1] = bb[best * L + j];
-        const int last = up[best * L + a];
-        if (!bad_len) {
-            if (last >= 0 && last < Pb) ot[a] = s_g[last];
-            else rd_flag(dev_status, RD_DEV_BAD_INDEX);
-        }
-        tickets[b] = 0u;
-    }
+    accept_request(b, P_max, V, Pb, bad_len, beams, unpacker, W, L, argmax_out, accept_len,
+                   best_beam, n_accepted, out_tokens, keys, tickets, dev_status, s_g, s_acc,
+                   s_bb, s_up);
 }
 
 }  // namespace
