@@ -59,6 +59,10 @@ def _args():
                     help="skip timing the calls beyond the verification step")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's request count (small profiling runs)")
+    ap.add_argument("--profile-case", default="",
+                    choices=["", "attention", "attention_fp8", "causal_all_ctx", "greedy_accept"],
+                    help="run only this call (warmup + steps launches, no JSON contract line): "
+                         "the commands the ncu summaries are taken with")
     return ap.parse_args()
 
 
@@ -256,6 +260,12 @@ def run_reference(args):
 # ----------------------------------------------------------------------------
 # our CUDA path
 # ----------------------------------------------------------------------------
+# A spin kernel of this many SM clocks (about 100 us) per call is queued ahead of
+# the timed calls, so that the host has enqueued them before the device reaches
+# them: the events then time the calls' device work, not the host's call overhead.
+_HOST_AHEAD_CYCLES = 200_000
+
+
 def _time_us(fn, n: int = 20) -> float:
     """Mean device time of one call, n calls back to back on the current stream
     (CUDA events, after three warm-up calls)."""
@@ -263,6 +273,7 @@ def _time_us(fn, n: int = 20) -> float:
         fn()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(_HOST_AHEAD_CYCLES * n)     # the device idles while the host enqueues
     e0.record()
     for _ in range(n):
         fn()
@@ -280,6 +291,7 @@ def _time_us_cold(fn, flush: torch.Tensor, n: int = 30) -> float:
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(n)]
     for e0, e1 in evs:
+        torch.cuda._sleep(_HOST_AHEAD_CYCLES)
         flush.zero_()
         e0.record()
         fn()
@@ -643,9 +655,72 @@ def run_ours(args):
         pg.destroy_process_group()
 
 
+def run_profile_case(args):
+    """One call of the path, repeated: --warmup untimed launches, then --steps more,
+    on the workload (--workload, --batch).  A profiler skips the warm-up launches
+    and captures the next one; the printed time is only a sanity figure."""
+    import tree_attention_verify_gb300 as rd
+    dev = torch.device("cuda", 0)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    case = args.profile_case
+    if case == "causal_all_ctx":
+        m = workloads.make_mixed_inputs("all_ctx", device=dev)
+        c = m["ctx"]
+        o = torch.empty_like(c["q"])
+        fn = lambda: rd.rd_causal_attention(c["q"], c["k"], c["v"], c["cu_seqlens"],  # noqa
+                                            max_seqlen=m["prefill_len"], out=o, dev_status=st)
+        name = f"in-flight batch, all context ({m['n_ctx']} x {m['prefill_len']} tokens)"
+    else:
+        cfg = _config(args)
+        inp = workloads.make_verify_inputs(cfg, device=dev)
+        pk = rd.rd_pack_beams(inp["beams"], cfg.P_max, dev_status=st)
+        max_ctx = max(1, int(inp["ctx_lens"].max()))
+        name = cfg.name
+        if case == "greedy_accept":
+            ws = torch.zeros(max(8, rd.rd_greedy_accept_workspace_size(cfg.B, cfg.P_max, cfg.vocab)),
+                             dtype=torch.uint8, device=dev)
+            acc = rd.rd_greedy_accept(inp["logits"], inp["beams"], pk["unpacker"], pk["packed_len"],
+                                      workspace=ws, dev_status=st)
+            fn = lambda: rd.rd_greedy_accept(inp["logits"], inp["beams"], pk["unpacker"],  # noqa
+                                             pk["packed_len"], out=acc, workspace=ws, dev_status=st)
+        else:
+            ws = torch.zeros(max(16, rd.rd_tree_attention_workspace_size(
+                cfg.B, cfg.P_max, cfg.Hq, cfg.Hkv, cfg.D, max_ctx, dev)), dtype=torch.uint8, device=dev)
+            o = torch.empty_like(inp["q"])
+            if case == "attention_fp8":
+                kc, ks = workloads.make_fp8_cache(inp["k_cache"])
+                vc, vs = workloads.make_fp8_cache(inp["v_cache"])
+                del inp["k_cache"], inp["v_cache"]
+                fn = lambda: rd.rd_tree_attention_fp8(  # noqa
+                    inp["q"], inp["k_draft"], inp["v_draft"], kc, vc, ks, vs, inp["ctx_offsets"],
+                    pk["packed_len"], pk["mask"], max_ctx=max_ctx, out=o, workspace=ws, dev_status=st)
+            else:
+                fn = lambda: rd.rd_tree_attention(  # noqa
+                    inp["q"], inp["k_draft"], inp["v_draft"], inp["k_cache"], inp["v_cache"],
+                    inp["ctx_offsets"], pk["packed_len"], pk["mask"], max_ctx=max_ctx, out=o,
+                    workspace=ws, dev_status=st)
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    if int(st.item()) != 0:
+        raise SystemExit(f"device status {int(st.item())}")
+    us = e0.elapsed_time(e1) * 1e3 / max(1, args.steps)
+    print(json.dumps({"profile_case": case, "workload": name, "launches": args.warmup + args.steps,
+                      "us_per_launch_warm": us}), flush=True)
+
+
 def main():
     args = _args()
-    if args.impl == "reference":
+    if args.profile_case:
+        run_profile_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

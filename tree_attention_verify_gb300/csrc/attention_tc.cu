@@ -11,28 +11,36 @@
 // h*G + r % G; causal: token t = r / G), so each K/V byte is read once per tile.
 // A unit walks its KV chunks (64 positions): the context (all visible, the last
 // chunk ragged), then the packed drafts (visible iff the node's ancestor-mask
-// bit is set).  CTAs take units round-robin in split-major order.
+// bit is set).  Persistent CTAs, two per SM, take units round-robin in
+// tile-major order.
 //
-// Warp roles (one CTA per SM, persistent over units):
+// Warp roles (256 threads; warpgroup 1 gives registers to warpgroup 0):
 //   warps 0-3  softmax: row r is TMEM lane r (a tile of <= 64 valid rows puts a
-//              row in two lanes, each taking half of a chunk's columns).  Write
-//              queries into TMEM (the next unit's into a second buffer before
-//              this unit's epilogue), turn S into 16-bit P in TMEM (online
-//              softmax in exp2 form, O rescaled only when a row maximum grows
-//              by more than 2^8), and write the output rows.
-//   warp 4     producer: TMA loads of K and V chunks (128-byte swizzle) into a
-//              ring of stages.
-//   warp 5     S issuer: S = Q K^T (M=128, N=chunk, K=D; A = Q in TMEM) into a
-//              double-buffered TMEM tile.
-//   warp 6     PV issuer: O += P V (M=128, N=D, K=chunk; A = P in TMEM) into TMEM;
-//              the two issuers run independently.
+//              row in two lanes, each taking half of a chunk's columns).  Turn S
+//              into 16-bit P written over S in TMEM (online softmax in exp2
+//              form, O rescaled only when a row maximum grows by more than 2^8),
+//              and write the output rows (staged through shared memory so that
+//              each store instruction covers whole 64-byte row segments).
+//   warp 4     producer: TMA loads (128-byte swizzle) of K and V chunks.
+//   warp 5     MMA issuer and TMEM owner: S = Q K^T (M=128, N=64, K=D) and
+//              O += P V (M=128, N=D, K=64; A = P in TMEM).
+//   warps 6-7  FP8: widen e4m3 chunks into the 16-bit ring; tree attention:
+//              warp 6 writes the query tiles into shared memory (TMA).
+// Tree attention (template flag PIPE) keeps two S tiles in TMEM and issues S of
+// chunk j+1 before PV of chunk j, so the tensor core computes the next scores
+// while the softmax warps work; its queries sit in shared memory and K and V
+// have separate rings (a K stage frees as soon as S has read it).  Causal
+// prefill and the FP8 path keep one S tile with the queries in TMEM (written by
+// the softmax warps) and issue S of a chunk right behind PV of the one before;
+// causal tiles have all 128 rows valid, and reading 32 KB of queries from shared
+// memory for every chunk's S measured slower there.
 // FP8 variant (template flag F8; context K/V stored as e4m3 with per-tensor
 // scales): the producer TMA-loads e4m3 context chunks into an 8-bit ring; warps
-// 6-9 widen them (exactly) into the 16-bit ring the MMA reads, and convert the
-// bf16 draft chunks, divided by the scales, the same way; warp 5 issues S and PV.
-// The MMA runs kind::f16 with f16 operands (e4m3 widens to f16 exactly; both operands
-// of one MMA share a type); the K scale is folded into the softmax scale, the V scale
-// into the output normalisation.
+// 6-7 widen them (exactly) into the 16-bit ring the MMA reads, and convert the
+// bf16 draft chunks, divided by the scales, the same way.  The MMA runs kind::f16
+// with f16 operands (e4m3 widens to f16 exactly; both operands of one MMA share
+// a type); the K scale is folded into the softmax scale, the V scale into the
+// output normalisation.
 // Every wait is bounded by a clock budget; on expiry the CTA records RD_DEV_TIMEOUT,
 // drains its in-flight copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
@@ -58,7 +66,7 @@ constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
 constexpr int kThreads = kSoftmaxThreads + 128;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;                // S and PV issuer and TMEM owner
-constexpr int kConvWarp0 = 6;              // FP8 only: converter warps 6 and 7
+constexpr int kConvWarp0 = 6;              // FP8: converter warps 6 and 7; else warp 6 writes queries
 // Register split (setmaxnreg): two CTAs of 256 threads share an SM, so each CTA
 // launches with 128 registers per thread, 32,768 in all; warpgroup 1 gives back
 // down to kRegsOther and the softmax warpgroup takes kRegsSoftmax:
@@ -73,29 +81,46 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when a max grows by > 2^8
 constexpr long long kWaitBudget = 4000000000LL;   // ~2 s of SM clock per wait
 
-template <int D, bool F8 = false> struct Cfg {
+template <int D, bool F8 = false, bool PIPE = false> struct Cfg {
+    // PIPE (16-bit tree attention) pipelines S: two S tiles in tensor memory, so
+    // that S of the next chunk is computed while the softmax warps work on this
+    // one, with the queries in shared memory.  Otherwise (causal prefill, whose
+    // 128-row tiles would re-read the queries from shared memory for every S MMA,
+    // and FP8, whose shared memory holds the 8-bit ring) one S tile and the
+    // queries in tensor memory.
+    static_assert(!(F8 && PIPE), "the FP8 path keeps one S tile");
+    static constexpr bool kPipe = PIPE;
     static constexpr int kNc = kN;                      // KV positions per chunk
     static constexpr int kDB = D / 64;                  // 64-element (128-byte) column blocks
-    // 16-bit ring and (FP8) 8-bit ring of context chunks, 96 KB per CTA
-    static constexpr int kStages = F8 ? 2 : (D == 128 ? 3 : 6);
+    static constexpr int kKBytes = kNc * D * 2;         // one K (or V) chunk
+    // PIPE: separate K and V rings (a K stage is free once S has read it, so K
+    // loads run ahead of the V loads) and the query tile.  Otherwise one ring of
+    // K + V stages (16-bit), and for FP8 the 8-bit ring of context chunks.
+    static constexpr int kStages = F8 ? 2 : PIPE ? (D == 128 ? 2 : 4) : (D == 128 ? 3 : 6);
     static constexpr int kF8Stages = F8 ? 2 : 0;
     static constexpr int kF8Ring = kF8Stages > 0 ? kF8Stages : 1;   // ring index modulus
-    static constexpr int kKBytes = kNc * D * 2;         // one K (or V) chunk
-    static constexpr int kStageBytes = 2 * kKBytes;
+    static constexpr int kStageBytes = PIPE ? kKBytes : 2 * kKBytes;
     static constexpr int kF8Bytes = 2 * kNc * D;        // one 8-bit K + V chunk
-    static constexpr int kStageOff = 0;
-    static constexpr int kF8Off = kStageOff + kStages * kStageBytes;
-    static constexpr int kBarOff = kF8Off + kF8Stages * kF8Bytes;
+    static constexpr int kStageOff = 0;                 // FP8: K + V stages; else K stages
+    static constexpr int kVOff = kStageOff + kStages * kStageBytes;    // V stages (16-bit path)
+    static constexpr int kF8Off = kVOff + (PIPE ? kStages * kKBytes : 0);
+    static constexpr int kQOff = kF8Off + kF8Stages * kF8Bytes;
+    static constexpr int kQBytes = kPipe ? kM * D * 2 : 0;             // [D / 64][128 rows][128 B]
+    // output staging: per softmax warp 32 rows x 64 bytes (32 bf16 columns)
+    static constexpr int kOStageOff = kQOff + kQBytes;
+    static constexpr int kOStageBytes = kSoftmaxWarps * 32 * 64;
+    static constexpr int kBarOff = kOStageOff + kOStageBytes;
     static constexpr int kSmemBytes = kBarOff + 512 + 1024;   // + barriers + alignment slack
+    static_assert(kSmemBytes <= 113 * 1024, "two CTAs per SM");
     // Tensor memory (32-bit columns x 128 lanes), a quarter of the SM's per CTA:
-    // the S tile, with P (16-bit pairs, the A operand of PV) written over its
-    // first half once S is in registers; the O accumulator; the tile's queries
-    // (16-bit pairs, the A operand of S).
+    // S tiles, with P (16-bit pairs, the A operand of PV) written over the first
+    // half of its tile once S is in registers; the O accumulator; (FP8) the
+    // tile's queries (16-bit pairs, the A operand of S).
     static constexpr uint32_t kTmemCols = 256;
-    static constexpr uint32_t kSCol = 0;                // kNc columns; P in [0, kNc / 2)
-    static constexpr uint32_t kOCol = kNc;              // D (<= 128) columns
-    static constexpr uint32_t kQCol = kOCol + 128;      // D / 2 (<= 64) columns
-    static_assert(kQCol + 64 <= kTmemCols, "tensor memory layout");
+    static constexpr uint32_t kSCol = 0;                // S tile b at kSCol + b * kNc
+    static constexpr uint32_t kOCol = kPipe ? 2 * kNc : kNc;   // D (<= 128) columns
+    static constexpr uint32_t kQCol = kOCol + 128;      // FP8: D / 2 (<= 64) columns
+    static_assert(kPipe ? kOCol + 128 <= kTmemCols : kQCol + 64 <= kTmemCols, "tensor memory layout");
 };
 
 struct TcArgs {
@@ -126,16 +151,23 @@ struct TcArgs {
     // failure-detection test hook: > 0 makes the MMA issuer first wait, with
     // this clock budget, on a barrier that nothing completes
     long long stall_budget;
+    // 16-bit path: the query tiles come by TMA (G a power of two <= 16) through
+    // map_q128 (boxes of 128 / G rows x G heads x 64 columns) and map_q16 (16 / G
+    // rows), else by plain loads of warp 6
+    bool q_tma;
 };
 
 struct Barriers {
-    uint64_t kv_full[8];
+    uint64_t kv_full[8];     // FP8: K + V stages; 16-bit path: K stages
     uint64_t kv_empty[8];
-    uint64_t s_full;         // S of the current chunk is in tensor memory
-    uint64_t p_full;         // P of the current chunk is written (softmax warps)
+    uint64_t v_full[4];      // 16-bit path: V stages
+    uint64_t v_empty[4];
+    uint64_t s_full[2];      // S of a chunk is in its tensor-memory tile (FP8: tile 0 only)
+    uint64_t pv_done[2];     // 16-bit path: PV of a chunk of that S tile has completed
+    uint64_t p_full[2];      // P of a chunk is written over its S tile (softmax warps)
     uint64_t o_final;        // PV of the unit's last chunk has completed
     uint64_t o_free;         // the epilogue has read O (softmax warps)
-    uint64_t q_full;         // the unit's queries are written (softmax warps)
+    uint64_t q_full;         // the unit's queries are written (FP8: softmax warps; else loader warps)
     uint64_t q_free;         // every S MMA of the unit has completed
     uint64_t drain;
     uint64_t f8_full[4];
@@ -302,6 +334,19 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, ok);
 }
 
+// The same wait with the waiting loop out of line: for a wait on the softmax
+// warps' hot path that rarely has to wait, so that the loop's registers are not
+// reserved there.
+__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort)
+{
+    return mbar_wait(bar, parity, abort, kWaitBudget);
+}
+__device__ __forceinline__ bool warp_wait_lean(uint64_t* bar, uint32_t parity, volatile int* abort)
+{
+    const bool ok = mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, abort);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // Combine the split partials of one output row:
 // out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.  The (m, l) of eight splits
 // are loaded together, and a split's (m, l) with the partial loads of half a row,
@@ -309,16 +354,19 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 // line: it runs once per row and unit, and inlining it into the kernel body
 // slowed the streaming loop of the single-split case.
 template <int D>
-__device__ __noinline__ void merge_split_row(const TcArgs& a, size_t prow, int n_splits,
+__device__ __noinline__ void merge_split_row(const TcArgs& a, size_t unit_id, int rr, int n_splits,
                                              bool valid, uint16_t* dst)
 {
     constexpr int NC = D / 2;                           // columns per pass
-    const float2* mlp = a.ml_part + prow * a.splits;
+    // partials of split s: row (unit_id * splits + s) * 128 + rr
+    const size_t stride = kM;                           // rows between splits
+    const size_t prow0 = unit_id * a.splits * kM + rr;
+    const float2* mlp = a.ml_part + prow0;
     float M = -INFINITY;
     for (int s0 = 0; valid && s0 < n_splits; s0 += 8) {
         float x[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] = s0 + i < n_splits ? __ldcg(&mlp[s0 + i].x) : -INFINITY;
+        for (int i = 0; i < 8; ++i) x[i] = s0 + i < n_splits ? __ldcg(&mlp[(s0 + i) * stride].x) : -INFINITY;
 #pragma unroll
         for (int i = 0; i < 8; ++i) M = fmaxf(M, x[i]);
     }
@@ -326,13 +374,13 @@ __device__ __noinline__ void merge_split_row(const TcArgs& a, size_t prow, int n
     float Ls = 0.f;
 #pragma unroll 1
     for (int half = 0; half < 2; ++half) {
-        const float* opp = a.o_part + prow * a.splits * D + half * NC;
+        const float* opp = a.o_part + prow0 * D + half * NC;
         float acc[NC];
 #pragma unroll
         for (int c = 0; c < NC; ++c) acc[c] = 0.f;
         for (int sp = 0; any && sp < n_splits; ++sp) {
-            const float2 ml = __ldcg(&mlp[sp]);
-            const float4* src = reinterpret_cast<const float4*>(opp + (size_t)sp * D);
+            const float2 ml = __ldcg(&mlp[sp * stride]);
+            const float4* src = reinterpret_cast<const float4*>(opp + (size_t)sp * stride * D);
             float4 x[NC / 4];
 #pragma unroll
             for (int i = 0; i < NC / 4; ++i) x[i] = __ldcg(src + i);
@@ -359,14 +407,16 @@ __device__ __noinline__ void merge_split_row(const TcArgs& a, size_t prow, int n
     }
 }
 
-template <int D, bool F8>
+template <int D, bool F8, bool PIPE>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map_kc,
                          const __grid_constant__ CUtensorMap map_vc,
                          const __grid_constant__ CUtensorMap map_kd,
-                         const __grid_constant__ CUtensorMap map_vd)
+                         const __grid_constant__ CUtensorMap map_vd,
+                         const __grid_constant__ CUtensorMap map_q128,
+                         const __grid_constant__ CUtensorMap map_q16)
 {
-    using C = Cfg<D, F8>;
+    using C = Cfg<D, F8, PIPE>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -380,17 +430,25 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
     if (tid == 0) {
         for (int i = 0; i < C::kStages; ++i) {
             mbar_init(&bar.kv_full[i], F8 ? 2 : 1);        // FP8: the two converter warps
-            mbar_init(&bar.kv_empty[i], 1);                // PV (after S) has read the stage
+            mbar_init(&bar.kv_empty[i], 1);                // FP8: PV (after S); else S has read K
+            if (C::kPipe) {
+                mbar_init(&bar.v_full[i], 1);
+                mbar_init(&bar.v_empty[i], 1);             // PV has read V
+            }
         }
         for (int i = 0; i < C::kF8Stages; ++i) {
             mbar_init(&bar.f8_full[i], 1);
             mbar_init(&bar.f8_empty[i], 2);
         }
-        mbar_init(&bar.s_full, 1);
-        mbar_init(&bar.p_full, kSoftmaxWarps);
+        mbar_init(&bar.s_full[0], 1);
+        mbar_init(&bar.s_full[1], 1);
+        mbar_init(&bar.pv_done[0], 1);
+        mbar_init(&bar.pv_done[1], 1);
+        mbar_init(&bar.p_full[0], kSoftmaxWarps);
+        mbar_init(&bar.p_full[1], kSoftmaxWarps);
         mbar_init(&bar.o_final, 1);
         mbar_init(&bar.o_free, kSoftmaxWarps);
-        mbar_init(&bar.q_full, kSoftmaxWarps);
+        mbar_init(&bar.q_full, C::kPipe ? 1 : kSoftmaxWarps);
         mbar_init(&bar.q_free, 1);
         mbar_init(&bar.drain, 1);
         mbar_init(&bar.grp, kSoftmaxWarps);
@@ -407,6 +465,10 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
         tma_prefetch_desc(&map_vc);
         tma_prefetch_desc(&map_kd);
         tma_prefetch_desc(&map_vd);
+        if (C::kPipe && a.q_tma) {
+            tma_prefetch_desc(&map_q128);
+            tma_prefetch_desc(&map_q16);
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -525,8 +587,175 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             }
             if (!ok) { fail(); break; }
         }
-    } else if (!F8 && warp == kProducerWarp) {
+    } else if (PIPE && warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
+        // K and V of the chunk sequence (every live unit's chunks in order) into
+        // their own rings.  K of chunk t is issued before V of chunk t - 1: a K
+        // stage comes free once S has read it, a V stage only once PV has, and S
+        // of a chunk runs ahead of PV of the chunk before.
+        if (lane == 0) {
+            struct Cursor {
+                int u, j, n, n_ctx, c_first, b, h;
+                int64_t kv_base;
+            };
+            auto seek = [&](Cursor& c, int u0) {          // the first live unit from u0 on
+                for (c.u = u0; c.u < a.n_units; c.u += gridDim.x) {
+                    const UnitGeo geo = unit_geo<C::kNc>(a, c.u);
+                    if (!geo.live) continue;
+                    c.j = 0;
+                    c.n = geo.n_ctx + geo.n_draft;
+                    c.n_ctx = geo.n_ctx;
+                    c.c_first = geo.c_first;
+                    c.b = geo.b;
+                    c.h = geo.h;
+                    c.kv_base = geo.kv_base;
+                    return;
+                }
+            };
+            auto advance = [&](Cursor& c) {
+                if (++c.j == c.n) seek(c, c.u + gridDim.x);
+            };
+            const bool paged = a.block_table != nullptr;
+            // tensor map and first row of chunk c.j: context (contiguous, or the page
+            // holding it), or the packed drafts
+            auto locate = [&](const Cursor& c, bool is_v, const CUtensorMap*& map) -> int {
+                if (c.j < c.n_ctx) {
+                    map = is_v ? &map_vc : &map_kc;
+                    const int pos0 = (c.c_first + c.j) * kN;
+                    if (!paged) return (int)(c.kv_base + pos0);
+                    int pg = __ldg(a.block_table + (size_t)c.b * a.max_pages + pos0 / a.page_size);
+                    if (pg < 0 || pg >= a.num_pages) {
+                        rd_flag(a.status, RD_DEV_BAD_INDEX);
+                        pg = 0;
+                    }
+                    return pg * a.page_size + pos0 % a.page_size;
+                }
+                map = is_v ? &map_vd : &map_kd;
+                return c.b * a.P_max + (c.j - c.n_ctx) * kN;
+            };
+            auto issue = [&](const Cursor& c, uint32_t g, bool is_v) -> bool {
+                const int st = g % C::kStages;
+                uint64_t* full = is_v ? &bar.v_full[st] : &bar.kv_full[st];
+                uint64_t* empty = is_v ? &bar.v_empty[st] : &bar.kv_empty[st];
+                if (g >= (uint32_t)C::kStages &&
+                    !mbar_wait(empty, ((g / C::kStages) - 1) & 1, abort, kWaitBudget))
+                    return false;
+                const CUtensorMap* map;
+                const int z = locate(c, is_v, map);
+                unsigned char* dst = smem + (is_v ? C::kVOff : C::kStageOff) + st * C::kKBytes;
+                mbar_arrive_expect_tx(full, C::kKBytes);
+#pragma unroll
+                for (int db = 0; db < C::kDB; ++db)
+                    tma_load_3d(dst + db * (kN * 128), map, full, db * 64, c.h, z);
+                return true;
+            };
+            Cursor ck, cv;
+            seek(ck, blockIdx.x);
+            cv = ck;
+            uint32_t gk = 0, gv = 0;                      // K and V chunks issued
+            while (!*abort) {
+                const bool k_more = ck.u < a.n_units;
+                const bool v_more = cv.u < a.n_units;
+                if (!k_more && !v_more) break;
+                if (k_more) {
+                    if (!issue(ck, gk, false)) { fail(); break; }
+                    advance(ck);
+                    ++gk;
+                }
+                if (v_more && (gv + 1 < gk || !k_more)) {
+                    if (!issue(cv, gv, true)) { fail(); break; }
+                    advance(cv);
+                    ++gv;
+                }
+            }
+            // drain: every issued copy must land before the CTA may exit
+            for (uint32_t k = gk > (uint32_t)C::kStages ? gk - C::kStages : 0u; k < gk; ++k)
+                mbar_wait(&bar.kv_full[k % C::kStages], (k / C::kStages) & 1, &no_abort, kWaitBudget);
+            for (uint32_t k = gv > (uint32_t)C::kStages ? gv - C::kStages : 0u; k < gv; ++k)
+                mbar_wait(&bar.v_full[k % C::kStages], (k / C::kStages) & 1, &no_abort, kWaitBudget);
+        }
+    } else if (PIPE && warp == kConvWarp0) {
+        // ------------------------------------------------------- query writer
+        // Each live unit's query tile into shared memory (the A operand of S,
+        // 128-byte swizzle), once every S MMA of the unit before has completed.
+        // Row m holds query row tile * 128 + m, or in a tile with at most 64 valid
+        // rows (paired lanes) row tile * 128 + 16 (m / 32) + m % 16, so that TMEM
+        // lanes m and m ^ 16 get the same scores.  With G a power of two <= 16 the
+        // tile is one TMA box per 64 columns (rows r = p G + g are G heads of
+        // consecutive positions), or eight 16-row boxes when paired; rows past the
+        // valid ones then hold whatever the tensor holds there (their scores are
+        // masked).  Otherwise the warp loads the rows (zeros past the valid ones).
+        // The next unit's boxes are prefetched into L2 when this unit's are issued.
+        auto q_row0 = [&](const UnitGeo& ug) -> int {   // tensor row of the tile's first position
+            const int p0 = ug.tile * (kM / a.G);
+            return a.causal ? (int)(ug.kv_base + p0) : ug.b * a.P_max + p0;
+        };
+        auto paired_of = [&](const UnitGeo& ug) { return ug.n_rows - ug.tile * kM <= 64; };
+        // TMA boxes of unit ug: fn(map, smem byte offset, x, y, z)
+        auto for_boxes = [&](const UnitGeo& ug, auto&& fn) {
+            const int z0 = q_row0(ug), y = ug.h * a.G;
+            if (!paired_of(ug)) {
+#pragma unroll
+                for (int db = 0; db < C::kDB; ++db) fn(&map_q128, db * (kM * 128), db * 64, y, z0);
+            } else {
+#pragma unroll 1
+                for (int k = 0; k < 8; ++k)                 // smem rows 16k.., query rows 16 (k / 2)..
+#pragma unroll
+                    for (int db = 0; db < C::kDB; ++db)
+                        fn(&map_q16, db * (kM * 128) + k * 16 * 128, db * 64, y, z0 + 16 * (k >> 1) / a.G);
+            }
+        };
+        auto q_src = [&](const UnitGeo& ug, int m) -> const uint4* {
+            const int qr = ug.tile * kM + (paired_of(ug) ? 16 * (m >> 5) + (m & 15) : m);
+            if (qr >= ug.n_rows) return nullptr;
+            const int qp = qr / a.G;
+            const size_t qrow = a.causal ? (size_t)(ug.kv_base + qp) : (size_t)ug.b * a.P_max + qp;
+            return reinterpret_cast<const uint4*>(a.q + (qrow * a.Hq + ug.h * a.G + qr % a.G) * D);
+        };
+        uint32_t it = 0;
+        for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
+            const UnitGeo geo = unit_geo<C::kNc>(a, u);
+            if (!geo.live) continue;
+            if (it > 0 && !warp_wait(&bar.q_free, (it - 1) & 1, abort, kWaitBudget)) { fail(); break; }
+            if (a.q_tma) {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bar.q_full, kM * D * 2);
+                    for_boxes(geo, [&](const CUtensorMap* map, int off, int x, int y, int z) {
+                        tma_load_3d(smem + C::kQOff + off, map, &bar.q_full, x, y, z);
+                    });
+                    if (u + (int)gridDim.x < a.n_units) {
+                        const UnitGeo nx = unit_geo<C::kNc>(a, u + gridDim.x);
+                        if (nx.live)
+                            for_boxes(nx, [&](const CUtensorMap* map, int, int x, int y, int z) {
+                                tma_prefetch_3d(map, x, y, z);
+                            });
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int m = lane; m < kM; m += 32) {
+                    const uint4* src = q_src(geo, m);
+#pragma unroll
+                    for (int db = 0; db < C::kDB; ++db) {
+                        uint4 v[8];
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) v[c] = src ? __ldg(src + db * 8 + c) : make_uint4(0, 0, 0, 0);
+                        unsigned char* dst = smem + C::kQOff + db * (kM * 128);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(dst + sw128(m, c)) = v[c];
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar.q_full);
+            }
+            ++it;
+        }
+        // drain: the last tile's copies must land before the CTA may exit
+        if (a.q_tma && lane == 0 && it > 0)
+            mbar_wait(&bar.q_full, (it - 1) & 1, &no_abort, kWaitBudget);
+    } else if (!F8 && !PIPE && warp == kProducerWarp) {
+        // ------------------------------------------------ producer (one K + V ring)
         if (lane == 0) {
             uint32_t g = 0;                               // global chunk counter
             for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
@@ -580,14 +809,16 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------- MMA issuer
-        // Per chunk: S = Q K^T into the S/P columns once the chunk has landed,
-        // right behind PV of the chunk before (whose A operand, P, lives in those
-        // columns: the MMAs of one thread run in issue order, so S writes them
-        // after PV has read them, and the commit behind S also tracks that PV);
-        // then, once the softmax warps have written P over S, O += P V.  After
-        // the last S of a unit, q_free tells the softmax warps that the queries
-        // may be overwritten; before the first PV of a unit (which restarts O),
-        // o_free that the epilogue of the unit before has read O.
+        // 16-bit path, per unit: S_0, then for each chunk j: S_{j+1} into the
+        // other S tile (behind PV_{j-1}, whose A operand, P, lives there: the MMAs
+        // of one thread run in issue order, so S writes the tile after PV has read
+        // it), then, once the softmax warps have written P_j, O += P_j V_j.  So
+        // the tensor core computes the next scores while the softmax warps work.
+        // FP8 path, per chunk: S_j right behind PV_{j-1} into the one S tile,
+        // then PV_j once P_j is written.
+        // After the last S of a unit, q_free tells the query writers that the
+        // queries may be overwritten; before the first PV of a unit (which
+        // restarts O), o_free that the epilogue of the unit before has read O.
         if (lane == 0) {
             constexpr uint32_t idS = F8 ? idesc_f16(kM, C::kNc, false, false) : idesc_bf16(kM, C::kNc, false, false);
             constexpr uint32_t idPV = F8 ? idesc_f16(kM, D, false, true) : idesc_bf16(kM, D, false, true);
@@ -596,8 +827,9 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             // (bits 0-13, address >> 4): build the base once and add offsets,
             // which keeps the issuing thread's work per MMA to two additions.
             const uint64_t k_desc = smem_desc(smem_addr(smem + C::kStageOff), 16, 1024, kSwizzle128B);
-            const uint64_t v_desc = smem_desc(smem_addr(smem + C::kStageOff + C::kKBytes), C::kNc * 128,
-                                              1024, kSwizzle128B);
+            const uint64_t v_desc = smem_desc(smem_addr(smem + (C::kPipe ? C::kVOff : C::kStageOff + C::kKBytes)),
+                                              C::kNc * 128, 1024, kSwizzle128B);
+            const uint64_t q_desc = smem_desc(smem_addr(smem + C::kQOff), 16, 1024, kSwizzle128B);
             if (a.stall_budget > 0 && !mbar_wait(&bar.never, 0, abort, a.stall_budget)) fail();
             for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
                 const UnitGeo geo = unit_geo<C::kNc>(a, u);
@@ -605,37 +837,88 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 const int n = geo.n_ctx + geo.n_draft;
                 if (!mbar_wait(&bar.q_full, unit_iter & 1, abort, kWaitBudget)) { fail(); break; }
                 bool ok = true;
-                for (int j = 0; j < n; ++j) {
-                    const uint32_t gg = g + j;
-                    const int st = (int)(gg % C::kStages);
-                    if (!mbar_wait(&bar.kv_full[st], (gg / C::kStages) & 1, abort, kWaitBudget)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    // D/16 K-steps into the S columns
-                    const uint64_t kd = k_desc + (uint64_t)((st * C::kStageBytes) >> 4);
+                if constexpr (C::kPipe) {
+                    // S_j: K-major Q (shared memory) times the K stage, D/16 K-steps
+                    auto issue_s = [&](int j) -> bool {
+                        const uint32_t gg = g + j;
+                        const int st = (int)(gg % C::kStages);
+                        if (!mbar_wait(&bar.kv_full[st], (gg / C::kStages) & 1, abort, kWaitBudget))
+                            return false;
+                        tc_fence_after();
+                        const uint64_t kd = k_desc + (uint64_t)((st * C::kKBytes) >> 4);
+                        const uint32_t sd = tmem + C::kSCol + (gg & 1) * C::kNc;
 #pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint32_t off = ((ks >> 2) * (C::kNc * 128) + (ks & 3) * 32) >> 4;
-                        mma_tmem_a(tmem + C::kSCol, tmem + C::kQCol + ks * 8, kd + off, idS, ks > 0);
-                    }
-                    mma_commit(&bar.s_full);
-                    if (j == n - 1) mma_commit(&bar.q_free);
-                    if (j == 0 && unit_iter > 0 &&
-                        !mbar_wait(&bar.o_free, (unit_iter - 1) & 1, abort, kWaitBudget)) {
-                        ok = false;
-                        break;
-                    }
-                    if (!mbar_wait(&bar.p_full, gg & 1, abort, kWaitBudget)) { ok = false; break; }
-                    tc_fence_after();
-                    // O += P V: K-steps of 16 positions, A = P over the S columns
-                    const uint64_t vd = v_desc + (uint64_t)((st * C::kStageBytes) >> 4);
+                        for (int ks = 0; ks < D / 16; ++ks) {
+                            const uint32_t a_off = ((ks >> 2) * (kM * 128) + (ks & 3) * 32) >> 4;
+                            const uint32_t b_off = ((ks >> 2) * (C::kNc * 128) + (ks & 3) * 32) >> 4;
+                            mma_smem_a(sd, q_desc + a_off, kd + b_off, idS, ks > 0);
+                        }
+                        mma_commit(&bar.kv_empty[st]);          // the K stage has been read
+                        mma_commit(&bar.s_full[gg & 1]);
+                        if (j == n - 1) mma_commit(&bar.q_free);
+                        return true;
+                    };
+                    ok = issue_s(0);
+                    for (int j = 0; ok && j < n; ++j) {
+                        if (j + 1 < n && !issue_s(j + 1)) { ok = false; break; }
+                        const uint32_t gg = g + j;
+                        const int st = (int)(gg % C::kStages);
+                        if (j == 0 && unit_iter > 0 &&
+                            !mbar_wait(&bar.o_free, (unit_iter - 1) & 1, abort, kWaitBudget)) {
+                            ok = false;
+                            break;
+                        }
+                        // one P barrier per S tile: the softmax warps may finish chunk
+                        // j + 1 (whose S is already issued) before this wait for P_j
+                        if (!mbar_wait(&bar.p_full[gg & 1], (gg >> 1) & 1, abort, kWaitBudget) ||
+                            !mbar_wait(&bar.v_full[st], (gg / C::kStages) & 1, abort, kWaitBudget)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        // O += P V: K-steps of 16 positions, A = P over S tile gg & 1
+                        const uint64_t vd = v_desc + (uint64_t)((st * C::kKBytes) >> 4);
+                        const uint32_t pa = tmem + C::kSCol + (gg & 1) * C::kNc;
 #pragma unroll
-                    for (int kk = 0; kk < C::kNc / 16; ++kk)
-                        mma_tmem_a(tmem + C::kOCol, tmem + C::kSCol + kk * 8,
-                                   vd + (uint64_t)((kk * 2048) >> 4), idPV, j > 0 || kk > 0);
-                    mma_commit(&bar.kv_empty[st]);
+                        for (int kk = 0; kk < C::kNc / 16; ++kk)
+                            mma_tmem_a(tmem + C::kOCol, pa + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), idPV,
+                                       j > 0 || kk > 0);
+                        mma_commit(&bar.v_empty[st]);
+                        mma_commit(&bar.pv_done[gg & 1]);
+                    }
+                } else {
+                    for (int j = 0; j < n; ++j) {
+                        const uint32_t gg = g + j;
+                        const int st = (int)(gg % C::kStages);
+                        if (!mbar_wait(&bar.kv_full[st], (gg / C::kStages) & 1, abort, kWaitBudget)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        // D/16 K-steps into the S columns
+                        const uint64_t kd = k_desc + (uint64_t)((st * C::kStageBytes) >> 4);
+#pragma unroll
+                        for (int ks = 0; ks < D / 16; ++ks) {
+                            const uint32_t off = ((ks >> 2) * (C::kNc * 128) + (ks & 3) * 32) >> 4;
+                            mma_tmem_a(tmem + C::kSCol, tmem + C::kQCol + ks * 8, kd + off, idS, ks > 0);
+                        }
+                        mma_commit(&bar.s_full[0]);
+                        if (j == n - 1) mma_commit(&bar.q_free);
+                        if (j == 0 && unit_iter > 0 &&
+                            !mbar_wait(&bar.o_free, (unit_iter - 1) & 1, abort, kWaitBudget)) {
+                            ok = false;
+                            break;
+                        }
+                        if (!mbar_wait(&bar.p_full[0], gg & 1, abort, kWaitBudget)) { ok = false; break; }
+                        tc_fence_after();
+                        // O += P V: K-steps of 16 positions, A = P over the S columns
+                        const uint64_t vd = v_desc + (uint64_t)((st * C::kStageBytes) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < C::kNc / 16; ++kk)
+                            mma_tmem_a(tmem + C::kOCol, tmem + C::kSCol + kk * 8,
+                                       vd + (uint64_t)((kk * 2048) >> 4), idPV, j > 0 || kk > 0);
+                        mma_commit(&bar.kv_empty[st]);
+                    }
                 }
                 if (!ok) { fail(); break; }
                 mma_commit(&bar.o_final);
@@ -732,16 +1015,20 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             // queries not written ahead (the first live unit, or one after a unit
             // that was not live): the S MMAs of the last live unit have completed,
             // as this warp waited for them at that unit's end
-            if (q_unit != u) load_q(geo);
+            if constexpr (!C::kPipe) {
+                if (q_unit != u) load_q(geo);
+            }
             float m = -INFINITY, l = 0.f;
             // a warp whose rows are all padding reads no scores; it writes zero P
             // rows (the S columns hold scores again every chunk)
             const bool dead = __all_sync(0xffffffffu, !valid);
             const uint32_t* mrow = (!a.causal && valid)
                 ? a.mask + ((size_t)geo.b * a.P_max + qpos) * a.mask_words : nullptr;
-            // One chunk: NCOL = 64 columns per lane, or 32 for a paired lane.  The
-            // commit that completed S_j also tracked PV_{j-1}, so O is stable here.
-            auto chunk = [&](auto ncol, int j) {
+            // One chunk (global index gg, S in the columns at sc): NCOL = 64 columns
+            // per lane, or 32 for a paired lane.  FP8: the commit that completed S_j
+            // also tracked PV_{j-1}, so O is stable here; 16-bit path: PV_{j-1} may
+            // still run, and a rescale of O first waits for it.
+            auto chunk = [&](auto ncol, int j, uint32_t gg, uint32_t sc) -> bool {
                 constexpr int NCOL = decltype(ncol)::value;
                 const int c0 = NCOL == 32 ? 32 * hf : 0;  // first column of this lane
                 float s[NCOL];
@@ -749,8 +1036,8 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                     // the load is warp-collective (one address for all lanes): read
                     // all 64 columns; a paired lane keeps its 32
                     uint32_t sr[64];
-                    tmem_ld32(s_col, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-                    tmem_ld32(s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+                    tmem_ld32(sc, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+                    tmem_ld32(sc + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
                     tmem_ld_wait();
 #pragma unroll
                     for (int c = 0; c < NCOL; ++c)
@@ -793,6 +1080,15 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 const bool need = ms > m + kRescaleThreshold;
                 const float m_new = need ? ms : m;
                 if (__any_sync(0xffffffffu, need) && j > 0) {
+                    if constexpr (C::kPipe) {
+                        // PV_{j-1} has completed: phase (gg - 1) / 2 of the barrier of
+                        // its S tile.  That barrier is at most one phase past it (PV_{j+1}
+                        // waits for P_{j+1}) and PV_{j-3} completed before S_j (issued
+                        // after it) did, so the parity names the phase.
+                        if (!warp_wait_lean(&bar.pv_done[(gg - 1) & 1], ((gg - 1) >> 1) & 1, abort))
+                            return false;
+                        tc_fence_after();
+                    }
                     const float alpha = need ? fast_exp2(m - m_new) : 1.f;
 #pragma unroll
                     for (int cb = 0; cb < D / 32; ++cb) {
@@ -825,47 +1121,53 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 // P (16-bit) over the first half of this lane's S columns, PV's A
                 // operand; a paired lane writes zeros over the other lane's columns
                 if constexpr (NCOL == 64) {
-                    tmem_st32(s_col, pv);
+                    tmem_st32(sc, pv);
                 } else {
                     uint32_t pw[32];
 #pragma unroll
                     for (int c = 0; c < 32; ++c) pw[c] = ((c >> 4) == hf) ? pv[c & 15] : 0u;
-                    tmem_st32(s_col, pw);
+                    tmem_st32(sc, pw);
                 }
                 l += ((lsum[0] + lsum[1]) + (lsum[2] + lsum[3])) +
                      ((lsum[4] + lsum[5]) + (lsum[6] + lsum[7]));
+                return true;
             };
             bool ok = true;
             for (int j = 0; j < n; ++j) {
                 const uint32_t gg = g + j;
-                if (!warp_wait(&bar.s_full, gg & 1, abort, kWaitBudget)) { ok = false; break; }
+                const int sb = C::kPipe ? (int)(gg & 1) : 0;            // S tile
+                const uint32_t sph = C::kPipe ? (gg >> 1) & 1 : gg & 1;  // its phase parity
+                const uint32_t sc = s_col + sb * C::kNc;
+                if (!warp_wait(&bar.s_full[sb], sph, abort, kWaitBudget)) { ok = false; break; }
                 tc_fence_after();
                 if (dead) {
                     uint32_t zero[32];
 #pragma unroll
                     for (int c = 0; c < 32; ++c) zero[c] = 0u;
-                    tmem_st32(s_col, zero);
+                    tmem_st32(sc, zero);
                 } else if (paired) {
-                    chunk(std::integral_constant<int, 32>{}, j);
+                    if (!chunk(std::integral_constant<int, 32>{}, j, gg, sc)) { ok = false; break; }
                 } else {
-                    chunk(std::integral_constant<int, 64>{}, j);
+                    if (!chunk(std::integral_constant<int, 64>{}, j, gg, sc)) { ok = false; break; }
                 }
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bar.p_full);
+                if (lane == 0) mbar_arrive(&bar.p_full[sb]);
             }
             // every S MMA of this unit has completed once q_free does; then the next
             // unit's queries (if it is live) go into the Q columns, so that its first
             // S MMA overlaps this unit's PV drain and epilogue
-            if (ok && !warp_wait(&bar.q_free, unit_iter & 1, abort, kWaitBudget)) ok = false;
-            if (ok && u + (int)gridDim.x < a.n_units) {
-                next_u = u + gridDim.x;
-                next_geo = unit_geo<C::kNc>(a, next_u);
-                if (next_geo.live) {
-                    tc_fence_after();
-                    load_q(next_geo);
-                    q_unit = next_u;
+            if constexpr (!C::kPipe) {
+                if (ok && !warp_wait(&bar.q_free, unit_iter & 1, abort, kWaitBudget)) ok = false;
+                if (ok && u + (int)gridDim.x < a.n_units) {
+                    next_u = u + gridDim.x;
+                    next_geo = unit_geo<C::kNc>(a, next_u);
+                    if (next_geo.live) {
+                        tc_fence_after();
+                        load_q(next_geo);
+                        q_unit = next_u;
+                    }
                 }
             }
             if (!ok || !warp_wait(&bar.o_final, unit_iter & 1, abort, kWaitBudget)) { fail(); break; }
@@ -874,24 +1176,49 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             // A paired row's O and l are the sums over its two lanes; lane half hf
             // then writes output columns [hf D/2, (hf + 1) D/2).
             const float l_row = paired ? l + __shfl_xor_sync(0xffffffffu, l, 16) : l;
-            auto o_block = [&](int cb, uint32_t (&o)[32]) {
-                tmem_ld32(o_col + cb * 32, o);
-                tmem_ld_wait();
-                if (paired) {
+            // O in registers (all blocks behind one wait); once read, the next
+            // unit's first PV may start
+            uint32_t ob[D / 32][32];
+#pragma unroll
+            for (int cb = 0; cb < D / 32; ++cb) tmem_ld32(o_col + cb * 32, ob[cb]);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.o_free);
+            if (paired) {
+#pragma unroll
+                for (int cb = 0; cb < D / 32; ++cb)
 #pragma unroll
                     for (int c = 0; c < 32; ++c)
-                        o[c] = __float_as_uint(__uint_as_float(o[c]) +
-                                               __shfl_xor_sync(0xffffffffu, __uint_as_float(o[c]), 16));
-                }
-            };
-            // O has been read: the next unit's first PV may start
-            auto release_o = [&]() {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar.o_free);
-            };
+                        ob[cb][c] = __float_as_uint(__uint_as_float(ob[cb][c]) +
+                                                    __shfl_xor_sync(0xffffffffu, __uint_as_float(ob[cb][c]), 16));
+            }
             auto mine = [&](int cb) { return !paired || (cb >= D / 64) == (hf == 1); };
             const bool split_mode = !a.causal && geo.n_splits > 1;
+            // Stores through the warp's staging slots, 64 bytes of a row per lane at
+            // a time: lane L puts its 4 chunks of 16 bytes in slot L (chunks rotated by
+            // (L / 2) % 4 against bank conflicts), then lane L stores chunk L % 4 of
+            // slots L / 4 + 8 i, so one store instruction covers 8 rows x 64 bytes
+            // instead of 32 rows x 16 bytes.  seg: where this lane's 64 bytes go.
+            unsigned char* stage = smem + C::kOStageOff + warp * (32 * 64);
+            auto slot_chunk = [](int sl, int c) { return sl * 64 + ((c ^ ((sl >> 1) & 3)) << 4); };
+            auto stage_store = [&](const uint4 (&v)[4], bool put, void* seg) {
+                if (put) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(stage + slot_chunk(lane, i)) = v[i];
+                }
+                const unsigned long long gp = put ? reinterpret_cast<unsigned long long>(seg) : 0ull;
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int sl = (lane >> 2) + 8 * i;
+                    const unsigned long long p = __shfl_sync(0xffffffffu, gp, sl);
+                    if (p != 0ull)
+                        reinterpret_cast<uint4*>(p)[lane & 3] =
+                            *reinterpret_cast<const uint4*>(stage + slot_chunk(sl, lane & 3));
+                }
+                __syncwarp();
+            };
             if (!split_mode) {
                 const float inv = (valid && l_row > 0.f) ? a.out_scale / l_row : 0.f;
                 const bool write = valid || (!a.causal && qpos < a.P_max);
@@ -901,22 +1228,20 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                                                  : (size_t)geo.b * a.P_max + qpos;
                     dst = a.o + (orow * a.Hq + hq0 + row % a.G) * D;
                 }
+                // bf16 rows, 32 columns (64 bytes) per pass
 #pragma unroll
                 for (int cb = 0; cb < D / 32; ++cb) {
-                    uint32_t o[32];
-                    o_block(cb, o);
-                    if (cb == D / 32 - 1) release_o();
-                    if (write && mine(cb)) {
+                    const uint32_t (&o)[32] = ob[cb];
+                    uint4 v[4];
 #pragma unroll
-                        for (int c = 0; c < 32; c += 8) {
-                            uint4 v;
-                            v.x = pack_bf16(__uint_as_float(o[c + 0]) * inv, __uint_as_float(o[c + 1]) * inv);
-                            v.y = pack_bf16(__uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv);
-                            v.z = pack_bf16(__uint_as_float(o[c + 4]) * inv, __uint_as_float(o[c + 5]) * inv);
-                            v.w = pack_bf16(__uint_as_float(o[c + 6]) * inv, __uint_as_float(o[c + 7]) * inv);
-                            *reinterpret_cast<uint4*>(dst + cb * 32 + c) = v;
-                        }
+                    for (int i = 0; i < 4; ++i) {
+                        const int c = 8 * i;
+                        v[i].x = pack_bf16(__uint_as_float(o[c + 0]) * inv, __uint_as_float(o[c + 1]) * inv);
+                        v[i].y = pack_bf16(__uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv);
+                        v[i].z = pack_bf16(__uint_as_float(o[c + 4]) * inv, __uint_as_float(o[c + 5]) * inv);
+                        v[i].w = pack_bf16(__uint_as_float(o[c + 6]) * inv, __uint_as_float(o[c + 7]) * inv);
                     }
+                    stage_store(v, write && mine(cb), dst + cb * 32);
                 }
                 // paired: rows 64-127 of the tile hold no valid row; their padded
                 // outputs are zero (half a row per lane)
@@ -931,42 +1256,48 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                     }
                 }
             } else {
-                // fp32 partials; the CTA that takes the last ticket of (b, h, tile) merges
+                // fp32 partials, split s of (b, h, tile) in rows
+                // (unit_id * splits + s) * 128 + r (each split's rows contiguous); the
+                // CTA that takes the last ticket of (b, h, tile) merges them
                 const size_t unit_id = ((size_t)geo.b * a.Hkv + geo.h) * a.tiles + geo.tile;
-                const size_t prow = unit_id * kM + r;
-                float* op = a.o_part + (prow * a.splits + geo.split) * D;
+                const size_t prow = (unit_id * a.splits + geo.split) * kM + r;
+                float* op = a.o_part + prow * D;
 #pragma unroll
                 for (int cb = 0; cb < D / 32; ++cb) {
-                    uint32_t o[32];
-                    o_block(cb, o);
-                    if (cb == D / 32 - 1) release_o();
-                    if (mine(cb)) {
 #pragma unroll
-                        for (int c = 0; c < 32; c += 4)
-                            *reinterpret_cast<float4*>(op + cb * 32 + c) =
-                                make_float4(__uint_as_float(o[c]), __uint_as_float(o[c + 1]),
-                                            __uint_as_float(o[c + 2]), __uint_as_float(o[c + 3]));
+                    for (int h2 = 0; h2 < 2; ++h2) {               // 16 columns (64 bytes) per pass
+                        uint4 v[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int c = 16 * h2 + 4 * i;
+                            v[i] = make_uint4(ob[cb][c], ob[cb][c + 1], ob[cb][c + 2], ob[cb][c + 3]);
+                        }
+                        stage_store(v, mine(cb), op + cb * 32 + 16 * h2);
                     }
                 }
-                if (hf == 0) a.ml_part[prow * a.splits + geo.split] = make_float2(m, l_row);
-                __threadfence();
+                if (hf == 0) a.ml_part[prow] = make_float2(m, l_row);
                 // The softmax warps meet on an mbarrier (a bounded wait, unlike a
-                // named barrier: a warp that gave up elsewhere cannot strand the others)
+                // named barrier: a warp that gave up elsewhere cannot strand the others).
+                // Thread 0's device-scope fence after that meeting publishes every
+                // softmax thread's partials before its ticket (the meeting orders
+                // them before the fence); after the ticket, its fence and the second
+                // meeting order the merging threads' reads after the other splits'.
                 if (!group_sync()) { fail(); break; }
                 if (tid == 0) {
+                    __threadfence();
                     const unsigned tk = atomicAdd(a.tickets + unit_id, 1u);
+                    __threadfence();
                     bar.last = (tk == (unsigned)geo.n_splits - 1u);
                 }
                 if (!group_sync()) { fail(); break; }
                 if (bar.last) {
-                    __threadfence();
                     // paired: lane half 1 writes the zero rows 64-127 of the tile
                     const int rr = hf == 0 ? r : 64 + r;
                     const int row_m = geo.tile * kM + rr;
                     const bool valid_m = hf == 0 && valid;
                     const int p = row_m / a.G;
                     if (p < a.P_max)
-                        merge_split_row<D>(a, unit_id * kM + rr, valid_m ? geo.n_splits : 0, valid_m,
+                        merge_split_row<D>(a, unit_id, rr, valid_m ? geo.n_splits : 0, valid_m,
                                            a.o + (((size_t)geo.b * a.P_max + p) * a.Hq + hq0 + row_m % a.G) * D);
                     if (tid == 0) a.tickets[unit_id] = 0u;
                 }
@@ -1017,6 +1348,25 @@ bool make_kv_map(CUtensorMap* map, const void* base, int64_t rows, int heads, in
     return r == CUDA_SUCCESS;
 }
 
+// queries [rows, Hq, D] bf16 -> boxes of box_rows positions x G heads x 64 columns,
+// 128-byte swizzle: a box lands as box_rows * G rows of 128 bytes, row p G + g
+bool make_q_map(CUtensorMap* map, const void* base, int64_t rows, int heads, int D, int G,
+                int box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    if (rows < 1) rows = 1;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)heads * D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)box_rows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // [rows, heads, D] e4m3 -> boxes of kNc (64) positions x 1 head x D bytes, 128-byte swizzle
 bool make_fp8_map(CUtensorMap* map, const void* base, int64_t rows, int heads, int D)
 {
@@ -1024,13 +1374,28 @@ bool make_fp8_map(CUtensorMap* map, const void* base, int64_t rows, int heads, i
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
     cuuint64_t strides[2] = {(cuuint64_t)D, (cuuint64_t)heads * D};
-    cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)Cfg<128, true>::kNc};
+    cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)kN};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// One launch of an instantiation (dynamic shared memory set per call: cheap, and
+// the attribute must be set on every device the library runs on).
+template <int D, bool F8, bool PIPE>
+cudaError_t launch(int grid, cudaStream_t stream, const TcArgs& a, const CUtensorMap& m0,
+                   const CUtensorMap& m1, const CUtensorMap& m2, const CUtensorMap& m3,
+                   const CUtensorMap& m4, const CUtensorMap& m5)
+{
+    using Cf = Cfg<D, F8, PIPE>;
+    cudaError_t e = cudaFuncSetAttribute(tree_attention_tc_kernel<D, F8, PIPE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    tree_attention_tc_kernel<D, F8, PIPE><<<grid, kThreads, Cf::kSmemBytes, stream>>>(a, m0, m1, m2, m3, m4, m5);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -1141,33 +1506,26 @@ cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, in
             !make_fp8_map(&mkc, fp8->k_cache, total_kv, Hkv, D) ||
             !make_fp8_map(&mvc, fp8->v_cache, total_kv, Hkv, D))
             return cudaErrorInvalidValue;
-        using Cf = Cfg<128, true>;
-        cudaError_t e = cudaFuncSetAttribute(tree_attention_tc_kernel<128, true>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Cf::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        tree_attention_tc_kernel<128, true><<<grid, kThreads, Cf::kSmemBytes, stream>>>(
-            a, mkc, mvc, mkc, mvc);
-        return cudaGetLastError();
+        a.q_tma = false;
+        return launch<128, true, false>(grid, stream, a, mkc, mvc, mkc, mvc, mkc, mvc);
     }
     if (!make_kv_map(&mkc, kc, kc_rows > 0 ? kc_rows : kd_rows, Hkv, D) ||
         !make_kv_map(&mvc, vc, kc_rows > 0 ? kc_rows : kd_rows, Hkv, D) ||
         !make_kv_map(&mkd, kd, kd_rows, Hkv, D) || !make_kv_map(&mvd, vd, kd_rows, Hkv, D))
         return cudaErrorInvalidValue;
-    if (D == 128) {
-        using Cf = Cfg<128>;
-        cudaError_t e = cudaFuncSetAttribute(tree_attention_tc_kernel<128, false>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Cf::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        tree_attention_tc_kernel<128, false><<<grid, kThreads, Cf::kSmemBytes, stream>>>(a, mkc, mvc, mkd, mvd);
-    } else {
-        using Cf = Cfg<64>;
-        cudaError_t e = cudaFuncSetAttribute(tree_attention_tc_kernel<64, false>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Cf::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        tree_attention_tc_kernel<64, false><<<grid, kThreads, Cf::kSmemBytes, stream>>>(a, mkc, mvc, mkd, mvd);
+    if (causal) {
+        a.q_tma = false;
+        return D == 128 ? launch<128, false, false>(grid, stream, a, mkc, mvc, mkd, mvd, mkc, mvc)
+                        : launch<64, false, false>(grid, stream, a, mkc, mvc, mkd, mvd, mkc, mvc);
     }
-    return cudaGetLastError();
+    // query tiles by TMA when a tile is whole boxes: G a power of two <= 16 (it
+    // divides the 16 rows of a paired box and the 128 of a tile)
+    CUtensorMap mq128, mq16;
+    const int64_t q_rows = (int64_t)B * P_max;
+    a.q_tma = a.G <= 16 && (a.G & (a.G - 1)) == 0 && (reinterpret_cast<uintptr_t>(q) & 15) == 0 &&
+              make_q_map(&mq128, q, q_rows, Hq, D, a.G, kM / a.G) &&
+              make_q_map(&mq16, q, q_rows, Hq, D, a.G, 16 / a.G);
+    if (!a.q_tma) { mq128 = mkc; mq16 = mkc; }
+    return D == 128 ? launch<128, false, true>(grid, stream, a, mkc, mvc, mkd, mvd, mq128, mq16)
+                    : launch<64, false, true>(grid, stream, a, mkc, mvc, mkd, mvd, mq128, mq16);
 }
