@@ -124,19 +124,23 @@ rd_status rd_pack_beams(const int32_t* beams, int B, int W, int L, int P_cap,
  * ctx_offsets int64 [B+1]               prefix sums of context lengths
  * total_ctx  rows of k_cache / v_cache (host-known; ctx_offsets[B] must not
  *            exceed it, else RD_DEV_BAD_LENGTH and that request is skipped)
- * max_ctx    bound on every context length (sizes the split-KV grid;
- *            a longer context sets RD_DEV_BAD_LENGTH and is skipped)
+ * max_ctx    bound on every context length (sizes the workspace; a longer
+ *            context sets RD_DEV_BAD_LENGTH and is skipped)
  * packed_len int32 [B]; mask uint32 [B, P_max, mask_words] as rd_pack_beams
  *            writes it (mask_words = ceil(P_max/32))
  * o          bf16 [B, P_max, Hq, D]
  * scale      softmax scale; <= 0 selects 1/sqrt(D)
- * workspace  device scratch of rd_tree_attention_workspace_size() bytes
- *            (split-KV partials and merge tickets).  It must be zero-filled
- *            before its first use; every call leaves its tickets at zero again
- *            (except a call that set RD_DEV_TIMEOUT: zero it again after one).
- *            Calls that share a workspace must not overlap in time.  The size
- *            depends on the SM count of the current device: query it with the
- *            device current that the call will run on.
+ * workspace  device scratch of rd_tree_attention_workspace_size() bytes: the
+ *            CTAs split the batch's KV chunks into equal ranges, and the fp32
+ *            partials of the units that a range boundary cuts go here, with one
+ *            descriptor per CTA naming the unit it merges (a second kernel,
+ *            launched on the same stream, merges them).  No initial contents are needed; every
+ *            call writes what it reads.  Calls that share a workspace must not
+ *            overlap in time.  The size depends on the SM count of the current
+ *            device: query it with the device current that the call will run
+ *            on.  A batch of at least two units (request, kv head, 128-row
+ *            tile) per CTA, or of B > 480, runs whole units round-robin and
+ *            needs none.
  * Supported: D in {64, 128}; Hq % Hkv == 0; 1 <= P_max <= RD_MAX_PACKED.
  */
 size_t rd_tree_attention_workspace_size(int B, int P_max, int Hq, int Hkv, int D,
@@ -338,8 +342,8 @@ rd_status rd_greedy_accept(const void* logits, int B, int P_max, int V,
  * clock cycles.  That wait runs out, the CTA records RD_DEV_TIMEOUT, its other
  * roles stop at their next wait, it waits (with the normal budget) for the
  * copies and MMAs it has issued, frees its tensor memory and returns.  The
- * outputs of such a launch are undefined, and its split-KV workspace must be
- * zeroed again.  budget_cycles <= 0 disarms it (the default).  Process-wide;
+ * outputs of such a launch are undefined; the next call needs nothing reset.
+ * budget_cycles <= 0 disarms it (the default).  Process-wide;
  * do not arm it while other threads launch attention they rely on.
  */
 void rd_debug_stall_attention(long long budget_cycles);

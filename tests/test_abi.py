@@ -77,10 +77,18 @@ def test_workspace_queries():
     import tree_attention_verify_gb300 as rd
     assert rd.rd_greedy_accept_workspace_size(64, 48, 32000) >= 64 * 48 * 8
     assert rd.rd_greedy_accept_workspace_size(0, 48, 32000) == 0
-    # a batch that already fills the GPU needs no split-KV workspace
+    # chunk-range division: per CTA two 128-row fp32 slots (O, m, l) for the pieces
+    # of cut units and a 16-byte merge descriptor
+    for B, P, Hq, Hkv, D, C in ((1, 20, 32, 32, 128, 2048), (16, 40, 32, 8, 128, 4096)):
+        n = rd.rd_tree_attention_workspace_size(B, P, Hq, Hkv, D, C)
+        per_cta = 2 * 128 * (D * 4 + 8) + 16
+        assert n > 0 and n % per_cta == 0
+    # a batch with at least two units (request, kv head, tile) per CTA runs whole
+    # units round-robin: no workspace
     assert rd.rd_tree_attention_workspace_size(64, 48, 40, 40, 128, 8192) == 0
-    # batch 1 is split along the context and needs partials
-    assert rd.rd_tree_attention_workspace_size(1, 20, 32, 32, 128, 2048) > 0
+    # too many requests for the per-request table in shared memory: whole units
+    # round-robin, no workspace
+    assert rd.rd_tree_attention_workspace_size(481, 20, 32, 32, 128, 2048) == 0
 
 
 def test_product_path_has_no_oracle_dependency():

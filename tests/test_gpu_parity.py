@@ -424,8 +424,9 @@ def test_tree_attention_maximum_packed_length():
 
 
 def test_tree_attention_reused_workspace_split_launches():
-    # every split-KV launch must leave the workspace's merge tickets at zero,
-    # so the same workspace gives the same results call after call
+    # the pieces of units cut by CTA boundaries go through the workspace; the
+    # merge reads only slots this call wrote, so a workspace full of NaN bit
+    # patterns (0xff bytes) gives the same result as a fresh one, call after call
     rd = _rd()
     cfg = workloads.CONFIGS["8b_gqa_b16"]
     inp = workloads.make_verify_inputs(cfg, device=DEV)
@@ -433,19 +434,17 @@ def test_tree_attention_reused_workspace_split_launches():
     pk = rd.rd_pack_beams(inp["beams"], cfg.P_max, dev_status=st)
     max_ctx = int(inp["ctx_lens"].max())
     n_ws = rd.rd_tree_attention_workspace_size(cfg.B, cfg.P_max, cfg.Hq, cfg.Hkv, cfg.D, max_ctx)
-    assert n_ws > 0                                      # this workload splits
-    ws = torch.zeros(n_ws, dtype=torch.uint8, device=DEV)
+    assert n_ws > 0                                      # this workload cuts units
     G = cfg.Hq // cfg.Hkv
-    tiles = -(-cfg.P_max * G // 128)
-    n_tail = cfg.B * cfg.Hkv * tiles * 4                 # the merge tickets end the workspace
     outs = []
-    for _ in range(3):
+    for fill in (0, 255, 255):
+        ws = torch.full((n_ws,), fill, dtype=torch.uint8, device=DEV)
         o = rd.rd_tree_attention(inp["q"], inp["k_draft"], inp["v_draft"], inp["k_cache"],
                                  inp["v_cache"], inp["ctx_offsets"], pk["packed_len"], pk["mask"],
                                  max_ctx=max_ctx, workspace=ws, dev_status=st)
         torch.cuda.synchronize()
         assert st.item() == 0
-        assert int(ws[-n_tail:].count_nonzero()) == 0
+        assert not torch.isnan(o.float()).any()
         outs.append(o.clone())
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
     rng = np.random.default_rng(5)

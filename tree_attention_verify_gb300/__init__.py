@@ -190,7 +190,8 @@ def rd_pack_beams(beams: torch.Tensor, P_cap: Optional[int] = None, *, out: Opti
 
 def rd_tree_attention_workspace_size(B: int, P_max: int, Hq: int, Hkv: int, D: int,
                                      max_ctx: int, device=None) -> int:
-    """Bytes of split-KV workspace; it depends on the SM count of the device the
+    """Bytes of attention workspace (partials of units cut by the CTAs' chunk
+    ranges, and the request table); it depends on the SM count of the device the
     call will run on (`device`, else the current device)."""
     if device is not None and torch.device(device).type == "cuda":
         with torch.cuda.device(device):
@@ -204,8 +205,8 @@ def rd_tree_attention(q, k_new, v_new, k_cache, v_cache, ctx_offsets, packed_len
     """Tree-masked attention of packed drafts (see rd_tree_attention in rd.h).
     q [B,P,Hq,D], k_new/v_new [B,P,Hkv,D], k_cache/v_cache [sum C,Hkv,D] bf16;
     ctx_offsets int64 [B+1]; packed_len int32 [B]; mask uint32/int32 [B,P,NW].
-    The workspace (if the plan needs one) must start zero-filled; it is returned
-    to zero by every call.  Pass the same workspace again to reuse it."""
+    The workspace (if the plan needs one) needs no initial contents; pass the
+    same workspace again to reuse it."""
     for n, t in (("q", q), ("k_new", k_new), ("v_new", v_new)):
         _need(t, n, torch.bfloat16, q.device, ndim=4)
     _need(k_cache, "k_cache", torch.bfloat16, q.device, ndim=3)
@@ -227,7 +228,7 @@ def rd_tree_attention(q, k_new, v_new, k_cache, v_cache, ctx_offsets, packed_len
         out = torch.empty_like(q)
     ws_need = rd_tree_attention_workspace_size(B, P, Hq, Hkv, D, max_ctx, q.device)
     if ws_need and workspace is None:
-        workspace = torch.zeros(ws_need, dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
     _run("rd_tree_attention", q,
         B, P, Hq, Hkv, D, float(scale), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
         _ptr(v_cache), _ptr(ctx_offsets), int(k_cache.shape[0]), int(max_ctx), _ptr(packed_len),
@@ -268,7 +269,7 @@ def rd_tree_attention_fp8(q, k_new, v_new, k_cache, v_cache, k_scale: float, v_s
         out = torch.empty_like(q)
     ws_need = rd_tree_attention_workspace_size(B, P, Hq, Hkv, D, max_ctx, q.device)
     if ws_need and workspace is None:
-        workspace = torch.zeros(ws_need, dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
     _run("rd_tree_attention_fp8", q,
         B, P, Hq, Hkv, D, float(scale), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
         _ptr(v_cache), float(k_scale), float(v_scale), _ptr(ctx_offsets),
@@ -306,7 +307,7 @@ def rd_tree_attention_paged(q, k_new, v_new, k_pool, v_pool, block_table, ctx_le
         out = torch.empty_like(q)
     ws_need = rd_tree_attention_workspace_size(B, P, Hq, Hkv, D, max_ctx, q.device)
     if ws_need and workspace is None:
-        workspace = torch.zeros(ws_need, dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
     _run("rd_tree_attention_paged", q,
         B, P, Hq, Hkv, D, float(scale), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool),
         _ptr(v_pool), n_pages, page_size, _ptr(block_table), block_table.shape[1],

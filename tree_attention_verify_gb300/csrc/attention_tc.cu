@@ -80,6 +80,8 @@ static_assert(32 * kCtasPerSm * (kRegsSoftmax + kRegsOther) <= 16384, "register 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when a max grows by > 2^8
 constexpr long long kWaitBudget = 4000000000LL;   // ~2 s of SM clock per wait
+constexpr int kSkMaxB = 480;               // chunk-range division up to this many requests
+constexpr uint32_t kSkMinChunks = 8;       // chunks per CTA at least (chunk-range division)
 
 template <int D, bool F8 = false, bool PIPE = false> struct Cfg {
     // PIPE (16-bit tree attention) pipelines S: two S tiles in tensor memory, so
@@ -90,6 +92,7 @@ template <int D, bool F8 = false, bool PIPE = false> struct Cfg {
     // queries in tensor memory.
     static_assert(!(F8 && PIPE), "the FP8 path keeps one S tile");
     static constexpr bool kPipe = PIPE;
+    static constexpr bool kMaySk = PIPE || F8;          // tree attention (chunk ranges possible)
     static constexpr int kNc = kN;                      // KV positions per chunk
     static constexpr int kDB = D / 64;                  // 64-element (128-byte) column blocks
     static constexpr int kKBytes = kNc * D * 2;         // one K (or V) chunk
@@ -110,7 +113,10 @@ template <int D, bool F8 = false, bool PIPE = false> struct Cfg {
     static constexpr int kOStageOff = kQOff + kQBytes;
     static constexpr int kOStageBytes = kSoftmaxWarps * 32 * 64;
     static constexpr int kBarOff = kOStageOff + kOStageBytes;
-    static constexpr int kSmemBytes = kBarOff + 512 + 1024;   // + barriers + alignment slack
+    // chunk-range table: per request the prefix of live chunks and chunks per unit
+    static constexpr int kSkOff = kBarOff + 512;
+    static constexpr int kSkBytes = (2 * kSkMaxB + 1) * 4;
+    static constexpr int kSmemBytes = kSkOff + kSkBytes + 1024;   // + alignment slack
     static_assert(kSmemBytes <= 113 * 1024, "two CTAs per SM");
     // Tensor memory (32-bit columns x 128 lanes), a quarter of the SM's per CTA:
     // S tiles, with P (16-bit pairs, the A operand of PV) written over the first
@@ -125,7 +131,13 @@ template <int D, bool F8 = false, bool PIPE = false> struct Cfg {
 
 struct TcArgs {
     bool causal;
-    int B, P_max, Hq, Hkv, G, tiles, splits, chunks_per_split, mask_words, n_units;
+    int B, P_max, Hq, Hkv, G, tiles, mask_words, n_units;   // n_units = B * Hkv * tiles
+    // Work division.  Chunk ranges (tree attention, B <= kSkMaxB): the live units'
+    // chunks, in request / tile / kv-head order, are one sequence of W chunks,
+    // and CTA c takes chunks [c W / grid, (c + 1) W / grid); a unit cut by such a
+    // boundary is computed in pieces whose fp32 partials the last piece to finish
+    // merges.  Otherwise whole units, round-robin in tile-major order.
+    bool sk;
     float scale_log2;
     const uint16_t* q;
     const int64_t* ctx_offsets;
@@ -136,7 +148,7 @@ struct TcArgs {
     uint16_t* o;
     float* o_part;
     float2* ml_part;
-    unsigned int* tickets;
+    int4* sk_desc;           // chunk ranges: per CTA, the cut unit its range starts inside (merge)
     int32_t* status;
     // paged context (block_table != nullptr): position j of request b is row
     // j % page_size of page block_table[b * max_pages + j / page_size]
@@ -172,74 +184,52 @@ struct Barriers {
     uint64_t drain;
     uint64_t f8_full[4];
     uint64_t f8_empty[4];
-    uint64_t grp;            // softmax warps' group sync in the split epilogue
     uint64_t never;          // completed by nobody (failure-detection test hook)
     uint32_t tmem_base;
     int abort;
-    int last;                // this CTA took the last ticket of a split unit
 };
 static_assert(sizeof(Barriers) <= 512, "barrier block");
 
-// Geometry of one work unit, computed identically by every role.
+// Geometry of one work item (a whole unit, or the piece of a unit that one CTA
+// takes), computed identically by every role.
 struct UnitGeo {
-    int b, h, tile, split;
-    bool live;            // has valid rows and this split exists
-    bool zero_tile;       // tree tile without valid rows: write zeros (split 0 only)
+    int b, h, tile;
+    bool live;            // has chunks to process
+    bool zero_tile;       // tree tile without valid rows: write zeros
     int n_rows;           // valid rows of (b, h)
     int64_t kv_base;      // first row of this request / sequence in the K/V map
     int C;                // context length (tree) or sequence length (causal)
     int Pb;               // packed length (tree)
     int c_first, n_ctx;   // first context chunk and number of context chunks
-    int n_draft;          // draft chunks (last split only)
-    int n_splits;
+    int d_first, n_draft; // first draft chunk and number of draft chunks
+    // a piece of a cut unit and its partial slot (2 blockIdx.x, or 2 blockIdx.x
+    // + 1 when the unit starts inside this CTA's range and runs past its end)
+    bool cut;
+    int split;
 };
 
-template <int NC>
-__device__ __forceinline__ UnitGeo unit_geo(const TcArgs& a, int u)
+// Lengths of request (or sequence) b; false (and zero lengths) if they are invalid.
+__device__ __forceinline__ bool req_geo(const TcArgs& a, int b, UnitGeo& g)
 {
-    UnitGeo g;
-    // Units run tile-major, then split, request and kv head: the CTAs take units
-    // round-robin, and this order puts the tiles past the valid rows of a tree
-    // batch (mostly padding) last instead of interleaving them with the live
-    // units, while the splits of one tile level and the long and short causal
-    // tiles still spread evenly over the CTAs.
-    const int bh = a.B * a.Hkv;
-    g.tile = u / (a.splits * bh);
-    const int rem = u % (a.splits * bh);
-    g.split = rem / bh;
-    g.b = (rem % bh) / a.Hkv;
-    g.h = rem % a.Hkv;
-    g.live = false;
-    g.zero_tile = false;
-    g.n_draft = 0;
-    g.n_ctx = 0;
-    g.c_first = 0;
-    g.n_splits = 1;
     bool bad;
     if (a.causal) {
-        const int s0 = a.lens[g.b], s1 = a.lens[g.b + 1];
+        const int s0 = a.lens[b], s1 = a.lens[b + 1];
         g.kv_base = s0;
         g.C = s1 - s0;
         g.Pb = 0;
         bad = s0 < 0 || g.C < 0 || g.C > a.max_kv || s1 > a.total_kv;
         if (bad) g.C = 0;
         g.n_rows = g.C * a.G;
-        const int row0 = g.tile * kM;
-        if (row0 < g.n_rows && g.split == 0) {
-            const int t_max = (min(g.n_rows, row0 + kM) - 1) / a.G;
-            g.n_ctx = t_max / NC + 1;
-            g.live = true;
-        }
     } else {
-        g.Pb = a.lens[g.b];
+        g.Pb = a.lens[b];
         if (a.block_table != nullptr) {
-            const int c = a.ctx_lens[g.b];
+            const int c = a.ctx_lens[b];
             g.kv_base = 0;
             g.C = c;
             bad = c < 0 || c > a.max_kv || (long long)c > (long long)a.max_pages * a.page_size ||
                   g.Pb < 0 || g.Pb > a.P_max;
         } else {
-            const int64_t c0 = a.ctx_offsets[g.b], c1 = a.ctx_offsets[g.b + 1];
+            const int64_t c0 = a.ctx_offsets[b], c1 = a.ctx_offsets[b + 1];
             g.kv_base = c0;
             g.C = (int)(c1 - c0);
             bad = c0 < 0 || c1 < c0 || c1 - c0 > a.max_kv || c1 > a.total_kv || g.Pb < 0 ||
@@ -247,21 +237,185 @@ __device__ __forceinline__ UnitGeo unit_geo(const TcArgs& a, int u)
         }
         if (bad) { g.C = 0; g.Pb = 0; }
         g.n_rows = g.Pb * a.G;
-        const int row0 = g.tile * kM;
-        const int n_cc = (g.C + NC - 1) / NC;
-        g.n_splits = max(1, (n_cc + a.chunks_per_split - 1) / a.chunks_per_split);
-        if (row0 >= g.n_rows) {
-            g.zero_tile = g.split == 0 && row0 < a.P_max * a.G;
-        } else if (g.split < g.n_splits) {
-            g.live = true;
-            g.c_first = g.split * a.chunks_per_split;
-            g.n_ctx = max(0, min(n_cc, g.c_first + a.chunks_per_split) - g.c_first);
-            if (g.split == g.n_splits - 1) g.n_draft = (g.Pb + NC - 1) / NC;
-        }
     }
-    if (bad && g.h == 0 && g.tile == 0 && g.split == 0 && threadIdx.x == 0)
-        rd_flag(a.status, RD_DEV_BAD_LENGTH);
+    return !bad;
+}
+
+// Whole unit u (round-robin division).  Units run tile-major, then request and
+// kv head: the CTAs take units round-robin, and this order puts the tiles past
+// the valid rows of a tree batch (mostly padding) last instead of interleaving
+// them with the live units, while the long and short causal tiles spread evenly
+// over the CTAs.
+template <int NC>
+__device__ __forceinline__ UnitGeo unit_geo(const TcArgs& a, int u)
+{
+    UnitGeo g;
+    const int bh = a.B * a.Hkv;
+    g.tile = u / bh;
+    g.b = (u % bh) / a.Hkv;
+    g.h = u % a.Hkv;
+    g.live = false;
+    g.zero_tile = false;
+    g.c_first = g.n_ctx = g.d_first = g.n_draft = 0;
+    g.cut = false;
+    g.split = 0;
+    const bool ok = req_geo(a, g.b, g);
+    const int row0 = g.tile * kM;
+    if (a.causal) {
+        if (row0 < g.n_rows) {
+            const int t_max = (min(g.n_rows, row0 + kM) - 1) / a.G;
+            g.n_ctx = t_max / NC + 1;
+            g.live = true;
+        }
+    } else if (row0 >= g.n_rows) {
+        g.zero_tile = row0 < a.P_max * a.G;
+    } else {
+        g.live = true;
+        g.n_ctx = (g.C + NC - 1) / NC;
+        g.n_draft = (g.Pb + NC - 1) / NC;
+    }
+    if (!ok && g.h == 0 && g.tile == 0 && threadIdx.x == 0) rd_flag(a.status, RD_DEV_BAD_LENGTH);
     return g;
+}
+
+// Chunk-range division over n = min(grid, W / kSkMinChunks) CTAs (at least one;
+// no range is empty, and none is so short that its pieces' partials and merge
+// cost more than the chunks): CTA c < n starts at chunk floor(c W / n).
+__device__ __forceinline__ uint32_t sk_ctas(uint32_t W)
+{
+    return max(1u, min((uint32_t)gridDim.x, W / kSkMinChunks));
+}
+__device__ __forceinline__ uint32_t sk_start(uint32_t W, int c)
+{
+    return (uint32_t)(((uint64_t)c * W) / sk_ctas(W));
+}
+
+// The table: pre[b] = live chunks of requests before b (pre[B] = W), nb[b] =
+// chunks of one unit of request b (its context and draft chunks; zero without
+// valid rows), tiles of request b = (pre[b + 1] - pre[b]) / (Hkv nb[b]).  Built by
+// one warp before the roles start.
+template <int NC>
+__device__ void sk_build(const TcArgs& a, uint32_t* pre, uint32_t* nb, int lane)
+{
+    uint32_t carry = 0;
+    for (int b0 = 0; b0 < a.B; b0 += 32) {
+        const int b = b0 + lane;
+        uint32_t w = 0;
+        if (b < a.B) {
+            UnitGeo g;
+            if (!req_geo(a, b, g)) rd_flag(a.status, RD_DEV_BAD_LENGTH);
+            const int tiles = (g.n_rows + kM - 1) / kM;
+            const uint32_t n = tiles > 0 ? (uint32_t)((g.C + NC - 1) / NC + (g.Pb + NC - 1) / NC) : 0u;
+            nb[b] = n;
+            w = (uint32_t)(a.Hkv * tiles) * n;
+        }
+        uint32_t incl = w;                                   // inclusive warp scan
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += y;
+        }
+        if (b < a.B) pre[b + 1] = carry + incl;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) pre[0] = 0;
+    __syncwarp();
+    // This CTA's merge descriptor: when its range starts inside a unit that began
+    // in the previous CTA's range, that unit is cut and this CTA names it for the
+    // merge kernel (unit id in tile-major order, its first CTA c0, its number of
+    // pieces, whether it starts inside c0's range, its request's packed length).
+    if (lane == 0) {
+        int4 d = make_int4(-1, 0, 0, 0);
+        const uint32_t W = carry;
+        const uint32_t n = W > 0 ? sk_ctas(W) : 0u;
+        const int c = blockIdx.x;
+        if (c >= 1 && (uint32_t)c < n) {
+            const uint32_t x = sk_start(W, c);
+            int lo = 0, hi = a.B - 1;                       // last b with pre[b] <= x
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (pre[mid] <= x) lo = mid; else hi = mid - 1;
+            }
+            const uint32_t n_b = nb[lo];
+            const uint32_t k = (x - pre[lo]) / n_b;
+            const uint32_t U0 = pre[lo] + k * n_b;
+            const uint32_t prev = sk_start(W, c - 1);
+            if (U0 < x && U0 >= prev) {
+                const int tile = (int)(k / a.Hkv), h = (int)(k % a.Hkv);
+                const uint32_t last = U0 + n_b - 1;
+                const int c1 = (int)((((uint64_t)last + 1) * n - 1) / W);
+                d.x = (tile * a.B + lo) * a.Hkv + h;
+                d.y = c - 1;
+                d.z = (c1 - (c - 1) + 1) | (U0 > prev ? (1 << 30) : 0);
+                d.w = a.lens[lo];
+            }
+        }
+        a.sk_desc[c] = d;
+    }
+}
+
+// Cursor over this CTA's work: a unit index (round-robin) or a chunk position.
+struct Work {
+    int u;
+    uint32_t x;
+};
+template <bool MAYSK>
+__device__ __forceinline__ Work work_begin(const TcArgs& a, const uint32_t* pre)
+{
+    Work w;
+    w.u = blockIdx.x;
+    w.x = 0u;
+    if (MAYSK && a.sk) {
+        const uint32_t W = pre[a.B];
+        w.x = blockIdx.x < sk_ctas(W) ? sk_start(W, blockIdx.x) : W;   // W: no work
+    }
+    return w;
+}
+
+// The CTA's next work item into g (round-robin: every unit, live or not; chunk
+// ranges: pieces of live units only); false when the CTA's work is done.
+template <int NC, bool MAYSK>
+__device__ __forceinline__ bool work_next(const TcArgs& a, const uint32_t* pre, const uint32_t* nb,
+                                          Work& w, UnitGeo& g)
+{
+    if (!(MAYSK && a.sk)) {
+        if (w.u >= a.n_units) return false;
+        g = unit_geo<NC>(a, w.u);
+        w.u += gridDim.x;
+        return true;
+    }
+    const uint32_t W = pre[a.B];
+    if (blockIdx.x >= sk_ctas(W)) return false;
+    const uint32_t end = sk_start(W, blockIdx.x + 1);
+    if (w.x >= end) return false;
+    int lo = 0, hi = a.B - 1;                               // last b with pre[b] <= x
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pre[mid] <= w.x) lo = mid; else hi = mid - 1;
+    }
+    const int b = lo;
+    const uint32_t n_b = nb[b];
+    const uint32_t k = (w.x - pre[b]) / n_b;                // unit of request b: (tile, kv head)
+    const uint32_t U0 = pre[b] + k * n_b;
+    const int cb = (int)(w.x - U0);
+    const int ce = (int)min(n_b, end - U0);
+    g.b = b;
+    g.tile = (int)(k / a.Hkv);
+    g.h = (int)(k % a.Hkv);
+    req_geo(a, b, g);
+    g.live = true;
+    g.zero_tile = false;
+    const int n_cc = (g.C + NC - 1) / NC;
+    g.c_first = min(cb, n_cc);
+    g.n_ctx = max(0, min(ce, n_cc) - cb);
+    g.d_first = max(cb, n_cc) - n_cc;
+    g.n_draft = max(0, ce - max(cb, n_cc));
+    g.cut = !(cb == 0 && ce == (int)n_b);
+    // the unit starts inside this CTA's range (not at its start) and is cut: the
+    // range's last piece, slot 2 c + 1; otherwise slot 2 c
+    g.split = 2 * (int)blockIdx.x + ((g.cut && cb == 0 && U0 > sk_start(W, blockIdx.x)) ? 1 : 0);
+    w.x = U0 + ce;
+    return true;
 }
 
 // Prefetch into L1 the per-request words that unit_geo will read for unit u, so
@@ -347,66 +501,6 @@ __device__ __forceinline__ bool warp_wait_lean(uint64_t* bar, uint32_t parity, v
     return __all_sync(0xffffffffu, ok);
 }
 
-// Combine the split partials of one output row:
-// out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.  The (m, l) of eight splits
-// are loaded together, and a split's (m, l) with the partial loads of half a row,
-// so a merge costs about one round trip per split and half row.  Kept out of
-// line: it runs once per row and unit, and inlining it into the kernel body
-// slowed the streaming loop of the single-split case.
-template <int D>
-__device__ __noinline__ void merge_split_row(const TcArgs& a, size_t unit_id, int rr, int n_splits,
-                                             bool valid, uint16_t* dst)
-{
-    constexpr int NC = D / 2;                           // columns per pass
-    // partials of split s: row (unit_id * splits + s) * 128 + rr
-    const size_t stride = kM;                           // rows between splits
-    const size_t prow0 = unit_id * a.splits * kM + rr;
-    const float2* mlp = a.ml_part + prow0;
-    float M = -INFINITY;
-    for (int s0 = 0; valid && s0 < n_splits; s0 += 8) {
-        float x[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] = s0 + i < n_splits ? __ldcg(&mlp[(s0 + i) * stride].x) : -INFINITY;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) M = fmaxf(M, x[i]);
-    }
-    const bool any = valid && M != -INFINITY;
-    float Ls = 0.f;
-#pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
-        const float* opp = a.o_part + prow0 * D + half * NC;
-        float acc[NC];
-#pragma unroll
-        for (int c = 0; c < NC; ++c) acc[c] = 0.f;
-        for (int sp = 0; any && sp < n_splits; ++sp) {
-            const float2 ml = __ldcg(&mlp[sp * stride]);
-            const float4* src = reinterpret_cast<const float4*>(opp + (size_t)sp * stride * D);
-            float4 x[NC / 4];
-#pragma unroll
-            for (int i = 0; i < NC / 4; ++i) x[i] = __ldcg(src + i);
-            const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
-            if (half == 0) Ls += ml.y * w;
-#pragma unroll
-            for (int i = 0; i < NC / 4; ++i) {
-                acc[4 * i + 0] += x[i].x * w;
-                acc[4 * i + 1] += x[i].y * w;
-                acc[4 * i + 2] += x[i].z * w;
-                acc[4 * i + 3] += x[i].w * w;
-            }
-        }
-        const float inv = (any && Ls > 0.f) ? a.out_scale / Ls : 0.f;
-#pragma unroll
-        for (int c = 0; c < NC; c += 8) {
-            uint4 v;
-            v.x = pack_bf16(acc[c + 0] * inv, acc[c + 1] * inv);
-            v.y = pack_bf16(acc[c + 2] * inv, acc[c + 3] * inv);
-            v.z = pack_bf16(acc[c + 4] * inv, acc[c + 5] * inv);
-            v.w = pack_bf16(acc[c + 6] * inv, acc[c + 7] * inv);
-            *reinterpret_cast<uint4*>(dst + half * NC + c) = v;
-        }
-    }
-}
-
 template <int D, bool F8, bool PIPE>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map_kc,
@@ -451,7 +545,6 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
         mbar_init(&bar.q_full, C::kPipe ? 1 : kSoftmaxWarps);
         mbar_init(&bar.q_free, 1);
         mbar_init(&bar.drain, 1);
-        mbar_init(&bar.grp, kSoftmaxWarps);
         mbar_init(&bar.never, 1);
         bar.abort = 0;
         mbar_fence_init();
@@ -459,6 +552,12 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
     if (warp == kMmaWarp) {
         tmem_alloc(&bar.tmem_base, C::kTmemCols);
         tmem_relinquish();
+    }
+    uint32_t* sk_pre = reinterpret_cast<uint32_t*>(smem + C::kSkOff);
+    uint32_t* sk_nb = sk_pre + kSkMaxB + 1;
+    // (causal prefill, the one-S-tile 16-bit instantiation, never divides by chunk ranges)
+    if constexpr (C::kMaySk) {
+        if (a.sk && warp == 0) sk_build<C::kNc>(a, sk_pre, sk_nb, lane);
     }
     if (warp == kProducerWarp && lane == 0) {
         tma_prefetch_desc(&map_kc);
@@ -488,8 +587,9 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
         // ------------------------------------------------- producer (8-bit context)
         if (lane == 0) {
             uint32_t g8 = 0;                              // context chunks only
-            for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
-                const UnitGeo geo = unit_geo<C::kNc>(a, u);
+            Work wk = work_begin<C::kMaySk>(a, sk_pre);
+            UnitGeo geo;
+            while (!*abort && work_next<C::kNc, C::kMaySk>(a, sk_pre, sk_nb, wk, geo)) {
                 if (!geo.live) continue;
                 bool ok = true;
                 for (int j = 0; j < geo.n_ctx; ++j, ++g8) {
@@ -550,8 +650,9 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 *reinterpret_cast<uint4*>(dst + (c >> 3) * (C::kNc * 128) + sw128(row, c & 7)) = y;
             }
         };
-        for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
-            const UnitGeo geo = unit_geo<C::kNc>(a, u);
+        Work wk = work_begin<C::kMaySk>(a, sk_pre);
+        UnitGeo geo;
+        while (!*abort && work_next<C::kNc, C::kMaySk>(a, sk_pre, sk_nb, wk, geo)) {
             if (!geo.live) continue;
             const int n = geo.n_ctx + geo.n_draft;
             bool ok = true;
@@ -571,7 +672,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                     ok = false;
                     break;
                 }
-                const int d = (j - geo.n_ctx) * C::kNc + row;       // draft row (drafts only)
+                const int d = (geo.d_first + j - geo.n_ctx) * C::kNc + row;   // draft row (drafts only)
                 if (ctx) {
                     widen_row(src, kdst);
                     widen_row(src + C::kNc * D, vdst);
@@ -595,17 +696,20 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
         // of a chunk runs ahead of PV of the chunk before.
         if (lane == 0) {
             struct Cursor {
-                int u, j, n, n_ctx, c_first, b, h;
+                Work w;
+                bool more;                                // positioned on a live item
+                int j, n, n_ctx, c_first, d_first, b, h;
                 int64_t kv_base;
             };
-            auto seek = [&](Cursor& c, int u0) {          // the first live unit from u0 on
-                for (c.u = u0; c.u < a.n_units; c.u += gridDim.x) {
-                    const UnitGeo geo = unit_geo<C::kNc>(a, c.u);
+            auto seek = [&](Cursor& c) {                  // the next live item from c.w on
+                UnitGeo geo;
+                while ((c.more = work_next<C::kNc, C::kMaySk>(a, sk_pre, sk_nb, c.w, geo))) {
                     if (!geo.live) continue;
                     c.j = 0;
                     c.n = geo.n_ctx + geo.n_draft;
                     c.n_ctx = geo.n_ctx;
                     c.c_first = geo.c_first;
+                    c.d_first = geo.d_first;
                     c.b = geo.b;
                     c.h = geo.h;
                     c.kv_base = geo.kv_base;
@@ -613,7 +717,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 }
             };
             auto advance = [&](Cursor& c) {
-                if (++c.j == c.n) seek(c, c.u + gridDim.x);
+                if (++c.j == c.n) seek(c);
             };
             const bool paged = a.block_table != nullptr;
             // tensor map and first row of chunk c.j: context (contiguous, or the page
@@ -631,7 +735,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                     return pg * a.page_size + pos0 % a.page_size;
                 }
                 map = is_v ? &map_vd : &map_kd;
-                return c.b * a.P_max + (c.j - c.n_ctx) * kN;
+                return c.b * a.P_max + (c.d_first + c.j - c.n_ctx) * kN;
             };
             auto issue = [&](const Cursor& c, uint32_t g, bool is_v) -> bool {
                 const int st = g % C::kStages;
@@ -649,13 +753,14 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                     tma_load_3d(dst + db * (kN * 128), map, full, db * 64, c.h, z);
                 return true;
             };
-            Cursor ck, cv;
-            seek(ck, blockIdx.x);
-            cv = ck;
+            Cursor ck;
+            ck.w = work_begin<C::kMaySk>(a, sk_pre);
+            seek(ck);
+            Cursor cv = ck;
             uint32_t gk = 0, gv = 0;                      // K and V chunks issued
             while (!*abort) {
-                const bool k_more = ck.u < a.n_units;
-                const bool v_more = cv.u < a.n_units;
+                const bool k_more = ck.more;
+                const bool v_more = cv.more;
                 if (!k_more && !v_more) break;
                 if (k_more) {
                     if (!issue(ck, gk, false)) { fail(); break; }
@@ -713,8 +818,9 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             return reinterpret_cast<const uint4*>(a.q + (qrow * a.Hq + ug.h * a.G + qr % a.G) * D);
         };
         uint32_t it = 0;
-        for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
-            const UnitGeo geo = unit_geo<C::kNc>(a, u);
+        Work wk = work_begin<C::kMaySk>(a, sk_pre);
+        UnitGeo geo;
+        while (!*abort && work_next<C::kNc, C::kMaySk>(a, sk_pre, sk_nb, wk, geo)) {
             if (!geo.live) continue;
             if (it > 0 && !warp_wait(&bar.q_free, (it - 1) & 1, abort, kWaitBudget)) { fail(); break; }
             if (a.q_tma) {
@@ -723,13 +829,12 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                     for_boxes(geo, [&](const CUtensorMap* map, int off, int x, int y, int z) {
                         tma_load_3d(smem + C::kQOff + off, map, &bar.q_full, x, y, z);
                     });
-                    if (u + (int)gridDim.x < a.n_units) {
-                        const UnitGeo nx = unit_geo<C::kNc>(a, u + gridDim.x);
-                        if (nx.live)
-                            for_boxes(nx, [&](const CUtensorMap* map, int, int x, int y, int z) {
-                                tma_prefetch_3d(map, x, y, z);
-                            });
-                    }
+                    Work w2 = wk;
+                    UnitGeo nx;
+                    if (work_next<C::kNc, C::kMaySk>(a, sk_pre, sk_nb, w2, nx) && nx.live)
+                        for_boxes(nx, [&](const CUtensorMap* map, int, int x, int y, int z) {
+                            tma_prefetch_3d(map, x, y, z);
+                        });
                 }
             } else {
 #pragma unroll 1
@@ -758,8 +863,9 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
         // ------------------------------------------------ producer (one K + V ring)
         if (lane == 0) {
             uint32_t g = 0;                               // global chunk counter
-            for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
-                const UnitGeo geo = unit_geo<C::kNc>(a, u);
+            Work wk = work_begin<C::kMaySk>(a, sk_pre);
+            UnitGeo geo;
+            while (!*abort && work_next<C::kNc, C::kMaySk>(a, sk_pre, sk_nb, wk, geo)) {
                 if (!geo.live) continue;
                 const int n = geo.n_ctx + geo.n_draft;
                 // first cache row of context chunk j (paged: looked up one chunk ahead,
@@ -793,7 +899,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                         z = paged ? this_row : (int)(geo.kv_base + (int64_t)(geo.c_first + j) * kN);
                     } else {
                         mk = &map_kd; mv = &map_vd;
-                        z = geo.b * a.P_max + (j - geo.n_ctx) * kN;
+                        z = geo.b * a.P_max + (geo.d_first + j - geo.n_ctx) * kN;
                     }
 #pragma unroll
                     for (int db = 0; db < C::kDB; ++db) {
@@ -831,8 +937,9 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                                               C::kNc * 128, 1024, kSwizzle128B);
             const uint64_t q_desc = smem_desc(smem_addr(smem + C::kQOff), 16, 1024, kSwizzle128B);
             if (a.stall_budget > 0 && !mbar_wait(&bar.never, 0, abort, a.stall_budget)) fail();
-            for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
-                const UnitGeo geo = unit_geo<C::kNc>(a, u);
+            Work wk = work_begin<C::kMaySk>(a, sk_pre);
+            UnitGeo geo;
+            while (!*abort && work_next<C::kNc, C::kMaySk>(a, sk_pre, sk_nb, wk, geo)) {
                 if (!geo.live) continue;
                 const int n = geo.n_ctx + geo.n_draft;
                 if (!mbar_wait(&bar.q_full, unit_iter & 1, abort, kWaitBudget)) { fail(); break; }
@@ -977,31 +1084,38 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar.q_full);
         };
-        uint32_t grp_uses = 0;
-        auto group_sync = [&]() -> bool {              // the softmax warps, bounded
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar.grp);
-            return warp_wait(&bar.grp, (grp_uses++) & 1, abort, kWaitBudget);
+        // zero output rows of tile `tile` of (b, h): a tree tile without valid rows
+        auto zero_tile = [&](int b, int h, int tile) {
+            const int row = tile * kM + tid;
+            const int p = row / a.G;
+            if (p < a.P_max) {
+                uint4* dst = reinterpret_cast<uint4*>(
+                    a.o + (((size_t)b * a.P_max + p) * a.Hq + h * a.G + row % a.G) * D);
+#pragma unroll
+                for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+            }
         };
         uint32_t g = 0, unit_iter = 0;
-        int q_unit = -1;                                   // unit whose queries are already written
-        int next_u = -1;                                   // unit whose geometry is in next_geo
+        bool q_ready = false;                              // (not PIPE) the next item's queries are written
+        Work wk = work_begin<C::kMaySk>(a, sk_pre);
+        UnitGeo geo;
+        bool have_next = false;                            // (not PIPE) the next item, looked up ahead
+        Work next_w;
         UnitGeo next_geo;
-        for (int u = blockIdx.x; u < a.n_units && !*abort; u += gridDim.x) {
-            const UnitGeo geo = next_u == u ? next_geo : unit_geo<C::kNc>(a, u);
+        while (!*abort) {
+            if (have_next) {
+                geo = next_geo;
+                wk = next_w;
+                have_next = false;
+            } else if (!work_next<C::kNc, C::kMaySk>(a, sk_pre, sk_nb, wk, geo)) {
+                break;
+            }
             // the words the next unit's geometry needs, into L1 now (its loads then
             // overlap this unit's chunks)
-            if (u + (int)gridDim.x < a.n_units) prefetch_geo(a, u + gridDim.x);
+            if (!(C::kMaySk && a.sk) && wk.u < a.n_units) prefetch_geo(a, wk.u);
             const int hq0 = geo.h * a.G;
             if (geo.zero_tile) {                           // padded rows of a tree tile
-                const int row = geo.tile * kM + tid;
-                const int p = row / a.G;
-                if (p < a.P_max) {
-                    uint4* dst = reinterpret_cast<uint4*>(
-                        a.o + (((size_t)geo.b * a.P_max + p) * a.Hq + hq0 + row % a.G) * D);
-#pragma unroll
-                    for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
-                }
+                zero_tile(geo.b, geo.h, geo.tile);
                 continue;
             }
             if (!geo.live) continue;
@@ -1016,7 +1130,8 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             // that was not live): the S MMAs of the last live unit have completed,
             // as this warp waited for them at that unit's end
             if constexpr (!C::kPipe) {
-                if (q_unit != u) load_q(geo);
+                if (!q_ready) load_q(geo);
+                q_ready = false;
             }
             float m = -INFINITY, l = 0.f;
             // a warp whose rows are all padding reads no scores; it writes zero P
@@ -1056,7 +1171,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                             if (pos0 + c >= lim) s[c] = -INFINITY;
                     }
                 } else {
-                    const int d0 = (j - geo.n_ctx) * C::kNc + c0;          // a multiple of 32
+                    const int d0 = (geo.d_first + j - geo.n_ctx) * C::kNc + c0;   // a multiple of 32
                     const uint32_t w0 = (d0 >> 5) < a.mask_words ? __ldg(mrow + (d0 >> 5)) : 0u;
                     const uint32_t w1 = (NCOL == 64 && (d0 >> 5) + 1 < a.mask_words)
                         ? __ldg(mrow + (d0 >> 5) + 1) : 0u;
@@ -1160,13 +1275,13 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             // S MMA overlaps this unit's PV drain and epilogue
             if constexpr (!C::kPipe) {
                 if (ok && !warp_wait(&bar.q_free, unit_iter & 1, abort, kWaitBudget)) ok = false;
-                if (ok && u + (int)gridDim.x < a.n_units) {
-                    next_u = u + gridDim.x;
-                    next_geo = unit_geo<C::kNc>(a, next_u);
+                next_w = wk;
+                if (ok && work_next<C::kNc, C::kMaySk>(a, sk_pre, sk_nb, next_w, next_geo)) {
+                    have_next = true;
                     if (next_geo.live) {
                         tc_fence_after();
                         load_q(next_geo);
-                        q_unit = next_u;
+                        q_ready = true;
                     }
                 }
             }
@@ -1194,7 +1309,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                                                     __shfl_xor_sync(0xffffffffu, __uint_as_float(ob[cb][c]), 16));
             }
             auto mine = [&](int cb) { return !paired || (cb >= D / 64) == (hf == 1); };
-            const bool split_mode = !a.causal && geo.n_splits > 1;
+            const bool split_mode = geo.cut;
             // Stores through the warp's staging slots, 64 bytes of a row per lane at
             // a time: lane L puts its 4 chunks of 16 bytes in slot L (chunks rotated by
             // (L / 2) % 4 against bank conflicts), then lane L stores chunk L % 4 of
@@ -1256,54 +1371,37 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                     }
                 }
             } else {
-                // fp32 partials, split s of (b, h, tile) in rows
-                // (unit_id * splits + s) * 128 + r (each split's rows contiguous); the
-                // CTA that takes the last ticket of (b, h, tile) merges them
-                const size_t unit_id = ((size_t)geo.b * a.Hkv + geo.h) * a.tiles + geo.tile;
-                const size_t prow = (unit_id * a.splits + geo.split) * kM + r;
-                float* op = a.o_part + prow * D;
+                // fp32 partials of this piece of a cut unit, in slot 2 blockIdx.x (or
+                // 2 blockIdx.x + 1 for a piece that ends the CTA's range after an
+                // earlier piece): O as float4 [slot][D / 4][128 rows], so that a
+                // warp's store covers consecutive rows, and (m, l) as [slot][128
+                // rows].  The merge kernel launched after this one combines them.
+                float4* op = reinterpret_cast<float4*>(a.o_part) + (size_t)geo.split * (D / 4) * kM + r;
 #pragma unroll
                 for (int cb = 0; cb < D / 32; ++cb) {
+                    if (mine(cb)) {
 #pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {               // 16 columns (64 bytes) per pass
-                        uint4 v[4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int c = 16 * h2 + 4 * i;
-                            v[i] = make_uint4(ob[cb][c], ob[cb][c + 1], ob[cb][c + 2], ob[cb][c + 3]);
-                        }
-                        stage_store(v, mine(cb), op + cb * 32 + 16 * h2);
+                        for (int q = 0; q < 8; ++q)
+                            op[(size_t)(cb * 8 + q) * kM] =
+                                make_float4(__uint_as_float(ob[cb][4 * q]), __uint_as_float(ob[cb][4 * q + 1]),
+                                            __uint_as_float(ob[cb][4 * q + 2]), __uint_as_float(ob[cb][4 * q + 3]));
                     }
                 }
-                if (hf == 0) a.ml_part[prow] = make_float2(m, l_row);
-                // The softmax warps meet on an mbarrier (a bounded wait, unlike a
-                // named barrier: a warp that gave up elsewhere cannot strand the others).
-                // Thread 0's device-scope fence after that meeting publishes every
-                // softmax thread's partials before its ticket (the meeting orders
-                // them before the fence); after the ticket, its fence and the second
-                // meeting order the merging threads' reads after the other splits'.
-                if (!group_sync()) { fail(); break; }
-                if (tid == 0) {
-                    __threadfence();
-                    const unsigned tk = atomicAdd(a.tickets + unit_id, 1u);
-                    __threadfence();
-                    bar.last = (tk == (unsigned)geo.n_splits - 1u);
-                }
-                if (!group_sync()) { fail(); break; }
-                if (bar.last) {
-                    // paired: lane half 1 writes the zero rows 64-127 of the tile
-                    const int rr = hf == 0 ? r : 64 + r;
-                    const int row_m = geo.tile * kM + rr;
-                    const bool valid_m = hf == 0 && valid;
-                    const int p = row_m / a.G;
-                    if (p < a.P_max)
-                        merge_split_row<D>(a, unit_id, rr, valid_m ? geo.n_splits : 0, valid_m,
-                                           a.o + (((size_t)geo.b * a.P_max + p) * a.Hq + hq0 + row_m % a.G) * D);
-                    if (tid == 0) a.tickets[unit_id] = 0u;
-                }
+                if (hf == 0) a.ml_part[(size_t)geo.split * kM + r] = make_float2(m, l_row);
             }
             g += n;
             ++unit_iter;
+        }
+        // chunk-range division: the tiles past each request's valid rows (the
+        // chunk ranges hold live units only), round-robin
+        if (C::kMaySk && a.sk && !*abort) {
+            const int bh = a.B * a.Hkv;
+            for (int idx = blockIdx.x; idx < a.n_units; idx += gridDim.x) {
+                const int tile = idx / bh, b = (idx % bh) / a.Hkv, h = idx % a.Hkv;
+                const uint32_t n_b = sk_nb[b];
+                const int tiles_b = n_b > 0 ? (int)((sk_pre[b + 1] - sk_pre[b]) / ((uint32_t)a.Hkv * n_b)) : 0;
+                if (tile >= tiles_b && tile * kM < a.P_max * a.G) zero_tile(b, h, tile);
+            }
         }
     }
 
@@ -1312,6 +1410,88 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+// Merge of the cut units (chunk-range division): CTA c merges the unit named by
+// attention CTA c's descriptor (a unit cut by the start of c's range that began
+// in c - 1's range; none: return).  512 threads: thread t takes tile row t % 128
+// and columns [D/4 (t / 128), +D/4).  The unit's pieces are those of CTAs
+// c0 .. c0 + n_seg - 1, piece s in slot 2 (c0 + s), except 2 c0 + 1 when the unit
+// starts inside c0's range; out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s
+// (M the largest m_s: a first pass over the pieces' m, then the sums, four
+// pieces' loads at a time).
+constexpr int kMergeThreads = 512;
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads)
+merge_pieces_kernel(const TcArgs a)
+{
+    constexpr int QC = D / 4;                           // columns per thread (D = 128: 32)
+    constexpr int NQ = QC / 4;                          // float4 per thread
+    const int4 dsc = a.sk_desc[blockIdx.x];
+    if (dsc.x < 0) return;
+    const int bh = a.B * a.Hkv;
+    const int tile = dsc.x / bh, b = (dsc.x % bh) / a.Hkv, h = dsc.x % a.Hkv;
+    const int c0 = dsc.y, n_seg = dsc.z & 0xffff;
+    const bool c0_last = (dsc.z >> 30) & 1;
+    const int r = threadIdx.x % kM, qc = threadIdx.x / kM;
+    const int row = tile * kM + r;
+    const int p = row / a.G;
+    if (p >= a.P_max) return;
+    uint16_t* dst = a.o + (((size_t)b * a.P_max + p) * a.Hq + h * a.G + row % a.G) * D + qc * QC;
+    const bool valid = row < dsc.w * a.G;
+    auto slot = [&](int sp) { return (sp == 0 && c0_last) ? 2 * c0 + 1 : 2 * (c0 + sp); };
+    float acc[QC];
+#pragma unroll
+    for (int c = 0; c < QC; ++c) acc[c] = 0.f;
+    float inv = 0.f;
+    if (valid) {
+        float M = -INFINITY;
+        for (int s0 = 0; s0 < n_seg; s0 += 8) {
+            float m8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                m8[i] = s0 + i < n_seg ? __ldcg(&a.ml_part[(size_t)slot(s0 + i) * kM + r].x) : -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) M = fmaxf(M, m8[i]);
+        }
+        float L = 0.f;
+        for (int s0 = 0; s0 < n_seg; s0 += 4) {
+            float2 ml[4];
+            float4 x[4][NQ];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const bool in = s0 + i < n_seg;
+                const size_t sl = in ? (size_t)slot(s0 + i) : 0;
+                ml[i] = in ? __ldcg(&a.ml_part[sl * kM + r]) : make_float2(-INFINITY, 0.f);
+                const float4* src = reinterpret_cast<const float4*>(a.o_part) + (sl * (D / 4) + qc * NQ) * kM + r;
+#pragma unroll
+                for (int q = 0; q < NQ; ++q)
+                    x[i][q] = in ? __ldcg(src + (size_t)q * kM) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float w = ml[i].x == -INFINITY ? 0.f : exp2f(ml[i].x - M);
+                L += ml[i].y * w;
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) {
+                    acc[4 * q + 0] += x[i][q].x * w;
+                    acc[4 * q + 1] += x[i][q].y * w;
+                    acc[4 * q + 2] += x[i][q].z * w;
+                    acc[4 * q + 3] += x[i][q].w * w;
+                }
+            }
+        }
+        inv = (M != -INFINITY && L > 0.f) ? a.out_scale / L : 0.f;
+    }
+#pragma unroll
+    for (int c = 0; c < QC; c += 8) {
+        uint4 v;
+        v.x = pack_bf16(acc[c + 0] * inv, acc[c + 1] * inv);
+        v.y = pack_bf16(acc[c + 2] * inv, acc[c + 3] * inv);
+        v.z = pack_bf16(acc[c + 4] * inv, acc[c + 5] * inv);
+        v.w = pack_bf16(acc[c + 6] * inv, acc[c + 7] * inv);
+        *reinterpret_cast<uint4*>(dst + c) = v;
     }
 }
 
@@ -1395,6 +1575,10 @@ cudaError_t launch(int grid, cudaStream_t stream, const TcArgs& a, const CUtenso
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmemBytes);
     if (e != cudaSuccess) return e;
     tree_attention_tc_kernel<D, F8, PIPE><<<grid, kThreads, Cf::kSmemBytes, stream>>>(a, m0, m1, m2, m3, m4, m5);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || !a.sk) return e;
+    // chunk-range division: merge the units that CTA boundaries cut
+    merge_pieces_kernel<D><<<grid, kMergeThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -1403,36 +1587,28 @@ cudaError_t launch(int grid, cudaStream_t stream, const TcArgs& a, const CUtenso
 rd_attn_plan rd_attn_make_plan(bool causal, int B, int P_max, int Hq, int Hkv, int D,
                                int max_kv)
 {
-    (void)D;
     rd_attn_plan plan;
     const int G = Hq / Hkv;
     const long rows = causal ? (long)max_kv * G : (long)P_max * G;
     plan.tiles = (int)((rows + kM - 1) / kM);
     if (plan.tiles < 1) plan.tiles = 1;
-    const long ctx_chunks = causal ? 1 : ((long)max_kv + kN - 1) / kN;
-    const long base_units = (long)B * Hkv * plan.tiles;
+    const long units = (long)B * Hkv * plan.tiles;
     const long ctas = (long)kCtasPerSm * rd_device_sm_count();
-    const long target = 3L * rd_device_sm_count();        // split units wanted: 3 per SM
-    long cps = ctx_chunks > 0 ? ctx_chunks : 1;           // context chunks per split
-    if (!causal && base_units < target && ctx_chunks > 4) {
-        long want = (target + base_units - 1) / base_units;
-        cps = (ctx_chunks + want - 1) / want;
-        if (cps < 4) cps = 4;                             // at least 256 positions per split
-    }
-    // a batch with fewer than two units per CTA: no unit longer than 4096
-    // positions, so that one long context does not hold up the launch
-    if (!causal && base_units < 2 * ctas && cps > 64) cps = 64;
-    plan.split_len = (int)(cps * kN);
-    plan.splits = causal ? 1 : (int)((ctx_chunks + cps - 1) / cps);
-    if (plan.splits < 1) plan.splits = 1;
-    if (plan.splits > 1) {
-        const size_t unit_rows = (size_t)B * Hkv * plan.tiles * kM;
-        plan.ws_bytes = unit_rows * plan.splits * (size_t)D * sizeof(float) +
-                        unit_rows * plan.splits * sizeof(float2) +
-                        (size_t)B * Hkv * plan.tiles * sizeof(unsigned int);
-    } else {
-        plan.ws_bytes = 0;
-    }
+    // chunk ranges for tree attention with fewer units than two per CTA (whole
+    // units round-robin leave most CTAs idle or hold the launch on the longest
+    // unit), while the request table fits in shared memory and the chunk count
+    // in 32 bits; a batch with more units balances well enough whole, and needs
+    // no partials, merge or workspace
+    const long unit_chunks = ((long)max_kv + kN - 1) / kN + ((long)P_max + kN - 1) / kN;
+    plan.stream_k = !causal && units < 2 * ctas && B <= kSkMaxB && units * unit_chunks < (1L << 31);
+    plan.grid = (int)(plan.stream_k ? ctas : std::min(units, ctas));
+    if (plan.grid < 1) plan.grid = 1;
+    // pieces of cut units: two 128-row fp32 slots (O and (m, l)) per CTA, then
+    // one merge descriptor per CTA
+    plan.ws_bytes = plan.stream_k
+        ? (size_t)2 * plan.grid * kM * ((size_t)D * sizeof(float) + sizeof(float2)) +
+              (size_t)plan.grid * sizeof(int4)
+        : 0;
     return plan;
 }
 
@@ -1459,10 +1635,9 @@ cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, in
     a.Hkv = Hkv;
     a.G = Hq / Hkv;
     a.tiles = plan.tiles;
-    a.splits = plan.splits;
-    a.chunks_per_split = plan.split_len / kN;
+    a.sk = plan.stream_k;
     a.mask_words = mask_words;
-    a.n_units = B * Hkv * plan.tiles * plan.splits;
+    a.n_units = B * Hkv * plan.tiles;
     a.scale_log2 = scale * kLog2e;
     a.q = static_cast<const uint16_t*>(q);
     a.ctx_offsets = ctx_offsets;
@@ -1474,7 +1649,7 @@ cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, in
     a.status = dev_status;
     a.o_part = nullptr;
     a.ml_part = nullptr;
-    a.tickets = nullptr;
+    a.sk_desc = nullptr;
     a.k_new = static_cast<const uint16_t*>(k_new);
     a.v_new = static_cast<const uint16_t*>(v_new);
     a.k_inv = a.v_inv = a.out_scale = 1.f;
@@ -1484,11 +1659,11 @@ cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, in
         a.out_scale = fp8->v_scale;
         a.scale_log2 *= fp8->k_scale;
     }
-    if (plan.splits > 1) {
-        const size_t unit_rows = (size_t)B * Hkv * plan.tiles * kM;
+    if (plan.stream_k) {
+        const size_t slot_rows = (size_t)2 * plan.grid * kM;
         a.o_part = static_cast<float*>(workspace);
-        a.ml_part = reinterpret_cast<float2*>(a.o_part + unit_rows * plan.splits * D);
-        a.tickets = reinterpret_cast<unsigned int*>(a.ml_part + unit_rows * plan.splits);
+        a.ml_part = reinterpret_cast<float2*>(a.o_part + slot_rows * D);
+        a.sk_desc = reinterpret_cast<int4*>(a.ml_part + slot_rows);
     }
     CUtensorMap mkc, mvc, mkd, mvd;
     const void* kc = causal ? k_new : k_cache;
@@ -1498,7 +1673,7 @@ cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, in
     const void* kd = causal ? k_new : k_new;
     const void* vd = causal ? v_new : v_new;
     if (kc == nullptr || kc_rows == 0) { kc = kd; vc = vd; }
-    const int grid = (int)std::min<long>((long)a.n_units, (long)kCtasPerSm * rd_device_sm_count());
+    const int grid = plan.grid;
     a.stall_budget = rd_attention_stall_budget();
     if (fp8 != nullptr) {
         // 8-bit context maps (the drafts are read by the converter warps)

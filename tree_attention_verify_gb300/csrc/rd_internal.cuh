@@ -60,9 +60,9 @@ cudaError_t rd_launch_sample_accept(const void* target, const void* draft, int B
 // Attention (tree and causal modes share one kernel family).
 struct rd_attn_plan {
     int tiles;         // row tiles per (request, kv head)
-    int splits;        // KV splits per (request, kv head, tile), grid upper bound
-    int split_len;     // KV positions per split (multiple of the chunk size)
-    size_t ws_bytes;   // workspace bytes needed
+    bool stream_k;     // chunk-range division (tree attention), else whole units round-robin
+    int grid;          // CTAs of the launch
+    size_t ws_bytes;   // workspace bytes needed (chunk ranges: partials of cut units)
 };
 struct rd_paged_kv {
     const int32_t* block_table;   // [B, max_pages]
