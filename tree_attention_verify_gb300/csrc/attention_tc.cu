@@ -99,7 +99,10 @@ template <int D, bool F8 = false, bool PIPE = false> struct Cfg {
     // PIPE: separate K and V rings (a K stage is free once S has read it, so K
     // loads run ahead of the V loads) and the query tile.  Otherwise one ring of
     // K + V stages (16-bit), and for FP8 the 8-bit ring of context chunks.
-    static constexpr int kStages = F8 ? 2 : PIPE ? (D == 128 ? 2 : 4) : (D == 128 ? 3 : 6);
+    // The 16-bit paths take their query tiles by TMA into shared memory (warp 6);
+    // the causal one then copies each into TMEM (tcgen05.cp) for S's A operand.
+    static constexpr bool kQTma = !F8;
+    static constexpr int kStages = F8 ? 2 : PIPE ? (D == 128 ? 2 : 4) : (D == 128 ? 2 : 5);
     static constexpr int kF8Stages = F8 ? 2 : 0;
     static constexpr int kF8Ring = kF8Stages > 0 ? kF8Stages : 1;   // ring index modulus
     static constexpr int kStageBytes = PIPE ? kKBytes : 2 * kKBytes;
@@ -108,7 +111,7 @@ template <int D, bool F8 = false, bool PIPE = false> struct Cfg {
     static constexpr int kVOff = kStageOff + kStages * kStageBytes;    // V stages (16-bit path)
     static constexpr int kF8Off = kVOff + (PIPE ? kStages * kKBytes : 0);
     static constexpr int kQOff = kF8Off + kF8Stages * kF8Bytes;
-    static constexpr int kQBytes = kPipe ? kM * D * 2 : 0;             // [D / 64][128 rows][128 B]
+    static constexpr int kQBytes = kQTma ? kM * D * 2 : 0;             // [D / 64][128 rows][128 B]
     // output staging: per softmax warp 32 rows x 64 bytes (32 bf16 columns)
     static constexpr int kOStageOff = kQOff + kQBytes;
     static constexpr int kOStageBytes = kSoftmaxWarps * 32 * 64;
@@ -542,7 +545,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
         mbar_init(&bar.p_full[1], kSoftmaxWarps);
         mbar_init(&bar.o_final, 1);
         mbar_init(&bar.o_free, kSoftmaxWarps);
-        mbar_init(&bar.q_full, C::kPipe ? 1 : kSoftmaxWarps);
+        mbar_init(&bar.q_full, C::kQTma ? 1 : kSoftmaxWarps);
         mbar_init(&bar.q_free, 1);
         mbar_init(&bar.drain, 1);
         mbar_init(&bar.never, 1);
@@ -564,7 +567,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
         tma_prefetch_desc(&map_vc);
         tma_prefetch_desc(&map_kd);
         tma_prefetch_desc(&map_vd);
-        if (C::kPipe && a.q_tma) {
+        if (C::kQTma && a.q_tma) {
             tma_prefetch_desc(&map_q128);
             tma_prefetch_desc(&map_q16);
         }
@@ -779,7 +782,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             for (uint32_t k = gv > (uint32_t)C::kStages ? gv - C::kStages : 0u; k < gv; ++k)
                 mbar_wait(&bar.v_full[k % C::kStages], (k / C::kStages) & 1, &no_abort, kWaitBudget);
         }
-    } else if (PIPE && warp == kConvWarp0) {
+    } else if (!F8 && warp == kConvWarp0) {
         // ------------------------------------------------------- query writer
         // Each live unit's query tile into shared memory (the A operand of S,
         // 128-byte swizzle), once every S MMA of the unit before has completed.
@@ -994,6 +997,20 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                         mma_commit(&bar.pv_done[gg & 1]);
                     }
                 } else {
+                    if constexpr (C::kQTma) {
+                        // the unit's query tile, landed in shared memory, into the Q
+                        // columns: D/16 copies of 128 rows x 16 values, the same K-steps
+                        // as an A operand read from shared memory.  They run in issue
+                        // order after the S MMAs of the unit before (which read the Q
+                        // columns), and the commit behind them frees the shared tile.
+                        tc_fence_after();
+#pragma unroll
+                        for (int ks = 0; ks < D / 16; ++ks) {
+                            const uint32_t a_off = ((ks >> 2) * (kM * 128) + (ks & 3) * 32) >> 4;
+                            tmem_cp_128x256b(tmem + C::kQCol + ks * 8, q_desc + a_off);
+                        }
+                        mma_commit(&bar.q_free);
+                    }
                     for (int j = 0; j < n; ++j) {
                         const uint32_t gg = g + j;
                         const int st = (int)(gg % C::kStages);
@@ -1010,7 +1027,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                             mma_tmem_a(tmem + C::kSCol, tmem + C::kQCol + ks * 8, kd + off, idS, ks > 0);
                         }
                         mma_commit(&bar.s_full[0]);
-                        if (j == n - 1) mma_commit(&bar.q_free);
+                        if (!C::kQTma && j == n - 1) mma_commit(&bar.q_free);
                         if (j == 0 && unit_iter > 0 &&
                             !mbar_wait(&bar.o_free, (unit_iter - 1) & 1, abort, kWaitBudget)) {
                             ok = false;
@@ -1129,7 +1146,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             // queries not written ahead (the first live unit, or one after a unit
             // that was not live): the S MMAs of the last live unit have completed,
             // as this warp waited for them at that unit's end
-            if constexpr (!C::kPipe) {
+            if constexpr (!C::kQTma) {
                 if (!q_ready) load_q(geo);
                 q_ready = false;
             }
@@ -1273,7 +1290,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             // every S MMA of this unit has completed once q_free does; then the next
             // unit's queries (if it is live) go into the Q columns, so that its first
             // S MMA overlaps this unit's PV drain and epilogue
-            if constexpr (!C::kPipe) {
+            if constexpr (!C::kQTma) {
                 if (ok && !warp_wait(&bar.q_free, unit_iter & 1, abort, kWaitBudget)) ok = false;
                 next_w = wk;
                 if (ok && work_next<C::kNc, C::kMaySk>(a, sk_pre, sk_nb, next_w, next_geo)) {
@@ -1688,19 +1705,17 @@ cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, in
         !make_kv_map(&mvc, vc, kc_rows > 0 ? kc_rows : kd_rows, Hkv, D) ||
         !make_kv_map(&mkd, kd, kd_rows, Hkv, D) || !make_kv_map(&mvd, vd, kd_rows, Hkv, D))
         return cudaErrorInvalidValue;
-    if (causal) {
-        a.q_tma = false;
-        return D == 128 ? launch<128, false, false>(grid, stream, a, mkc, mvc, mkd, mvd, mkc, mvc)
-                        : launch<64, false, false>(grid, stream, a, mkc, mvc, mkd, mvd, mkc, mvc);
-    }
     // query tiles by TMA when a tile is whole boxes: G a power of two <= 16 (it
     // divides the 16 rows of a paired box and the 128 of a tile)
     CUtensorMap mq128, mq16;
-    const int64_t q_rows = (int64_t)B * P_max;
+    const int64_t q_rows = causal ? total_kv : (int64_t)B * P_max;
     a.q_tma = a.G <= 16 && (a.G & (a.G - 1)) == 0 && (reinterpret_cast<uintptr_t>(q) & 15) == 0 &&
               make_q_map(&mq128, q, q_rows, Hq, D, a.G, kM / a.G) &&
               make_q_map(&mq16, q, q_rows, Hq, D, a.G, 16 / a.G);
     if (!a.q_tma) { mq128 = mkc; mq16 = mkc; }
+    if (causal)
+        return D == 128 ? launch<128, false, false>(grid, stream, a, mkc, mvc, mkd, mvd, mq128, mq16)
+                        : launch<64, false, false>(grid, stream, a, mkc, mvc, mkd, mvd, mq128, mq16);
     return D == 128 ? launch<128, false, true>(grid, stream, a, mkc, mvc, mkd, mvd, mq128, mq16)
                     : launch<64, false, true>(grid, stream, a, mkc, mvc, mkd, mvd, mq128, mq16);
 }

@@ -158,6 +158,13 @@ __device__ __forceinline__ void mma_smem_a(uint32_t d_tmem, uint64_t a_desc, uin
         : "memory");
 }
 
+// Copy a 128-row x 32-byte matrix from shared memory (by descriptor, as an MMA
+// operand) into TMEM: row r to lane r, 8 consecutive 32-bit columns from taddr.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t s_desc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+}
+
 // Arrive on an mbarrier once every tcgen05 operation issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint64_t* bar)
 {
