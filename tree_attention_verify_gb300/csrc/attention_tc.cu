@@ -19,21 +19,21 @@
 //              row in two lanes, each taking half of a chunk's columns).  Turn S
 //              into 16-bit P written over S in TMEM (online softmax in exp2
 //              form, O rescaled only when a row maximum grows by more than 2^8),
-//              and write the output rows (staged through shared memory so that
-//              each store instruction covers whole 64-byte row segments).
+//              and write the output rows.
 //   warp 4     producer: TMA loads (128-byte swizzle) of K and V chunks.
 //   warp 5     MMA issuer and TMEM owner: S = Q K^T (M=128, N=64, K=D) and
 //              O += P V (M=128, N=D, K=64; A = P in TMEM).
-//   warps 6-7  FP8: widen e4m3 chunks into the 16-bit ring; tree attention:
-//              warp 6 writes the query tiles into shared memory (TMA).
+//   warps 6-7  FP8: widen e4m3 chunks into the 16-bit ring; 16-bit paths:
+//              warp 6 loads the query tiles into shared memory (TMA).
 // Tree attention (template flag PIPE) keeps two S tiles in TMEM and issues S of
 // chunk j+1 before PV of chunk j, so the tensor core computes the next scores
 // while the softmax warps work; its queries sit in shared memory and K and V
 // have separate rings (a K stage frees as soon as S has read it).  Causal
-// prefill and the FP8 path keep one S tile with the queries in TMEM (written by
-// the softmax warps) and issue S of a chunk right behind PV of the one before;
-// causal tiles have all 128 rows valid, and reading 32 KB of queries from shared
-// memory for every chunk's S measured slower there.
+// prefill and the FP8 path keep one S tile with the queries in TMEM and issue S
+// of a chunk right behind PV of the one before: causal tiles have all 128 rows
+// valid, and reading 32 KB of queries from shared memory for every chunk's S
+// measured slower there, so the issuer copies each unit's shared-memory query
+// tile into TMEM once (tcgen05.cp); the FP8 softmax warps write theirs.
 // FP8 variant (template flag F8; context K/V stored as e4m3 with per-tensor
 // scales): the producer TMA-loads e4m3 context chunks into an 8-bit ring; warps
 // 6-7 widen them (exactly) into the 16-bit ring the MMA reads, and convert the
@@ -112,10 +112,7 @@ template <int D, bool F8 = false, bool PIPE = false> struct Cfg {
     static constexpr int kF8Off = kVOff + (PIPE ? kStages * kKBytes : 0);
     static constexpr int kQOff = kF8Off + kF8Stages * kF8Bytes;
     static constexpr int kQBytes = kQTma ? kM * D * 2 : 0;             // [D / 64][128 rows][128 B]
-    // output staging: per softmax warp 32 rows x 64 bytes (32 bf16 columns)
-    static constexpr int kOStageOff = kQOff + kQBytes;
-    static constexpr int kOStageBytes = kSoftmaxWarps * 32 * 64;
-    static constexpr int kBarOff = kOStageOff + kOStageBytes;
+    static constexpr int kBarOff = kQOff + kQBytes;
     // chunk-range table: per request the prefix of live chunks and chunks per unit
     static constexpr int kSkOff = kBarOff + 512;
     static constexpr int kSkBytes = (2 * kSkMaxB + 1) * 4;
@@ -1327,30 +1324,6 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             }
             auto mine = [&](int cb) { return !paired || (cb >= D / 64) == (hf == 1); };
             const bool split_mode = geo.cut;
-            // Stores through the warp's staging slots, 64 bytes of a row per lane at
-            // a time: lane L puts its 4 chunks of 16 bytes in slot L (chunks rotated by
-            // (L / 2) % 4 against bank conflicts), then lane L stores chunk L % 4 of
-            // slots L / 4 + 8 i, so one store instruction covers 8 rows x 64 bytes
-            // instead of 32 rows x 16 bytes.  seg: where this lane's 64 bytes go.
-            unsigned char* stage = smem + C::kOStageOff + warp * (32 * 64);
-            auto slot_chunk = [](int sl, int c) { return sl * 64 + ((c ^ ((sl >> 1) & 3)) << 4); };
-            auto stage_store = [&](const uint4 (&v)[4], bool put, void* seg) {
-                if (put) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(stage + slot_chunk(lane, i)) = v[i];
-                }
-                const unsigned long long gp = put ? reinterpret_cast<unsigned long long>(seg) : 0ull;
-                __syncwarp();
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int sl = (lane >> 2) + 8 * i;
-                    const unsigned long long p = __shfl_sync(0xffffffffu, gp, sl);
-                    if (p != 0ull)
-                        reinterpret_cast<uint4*>(p)[lane & 3] =
-                            *reinterpret_cast<const uint4*>(stage + slot_chunk(sl, lane & 3));
-                }
-                __syncwarp();
-            };
             if (!split_mode) {
                 const float inv = (valid && l_row > 0.f) ? a.out_scale / l_row : 0.f;
                 const bool write = valid || (!a.causal && qpos < a.P_max);
@@ -1360,7 +1333,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                                                  : (size_t)geo.b * a.P_max + qpos;
                     dst = a.o + (orow * a.Hq + hq0 + row % a.G) * D;
                 }
-                // bf16 rows, 32 columns (64 bytes) per pass
+                // bf16 rows, 32 columns (64 bytes) at a time, each lane its own row
 #pragma unroll
                 for (int cb = 0; cb < D / 32; ++cb) {
                     const uint32_t (&o)[32] = ob[cb];
@@ -1373,7 +1346,10 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                         v[i].z = pack_bf16(__uint_as_float(o[c + 4]) * inv, __uint_as_float(o[c + 5]) * inv);
                         v[i].w = pack_bf16(__uint_as_float(o[c + 6]) * inv, __uint_as_float(o[c + 7]) * inv);
                     }
-                    stage_store(v, write && mine(cb), dst + cb * 32);
+                    if (write && mine(cb)) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) reinterpret_cast<uint4*>(dst + cb * 32)[i] = v[i];
+                    }
                 }
                 // paired: rows 64-127 of the tile hold no valid row; their padded
                 // outputs are zero (half a row per lane)
