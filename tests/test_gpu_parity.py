@@ -315,6 +315,43 @@ def test_tree_attention_ragged_and_empty_context(ctx):
     _attention_case(workloads.make_verify_inputs(cfg, device="cpu", ctx_override=ctx))
 
 
+def test_tree_attention_zero_and_bad_packed_lengths():
+    # a small batch runs on chunk ranges: a request with no packed nodes owns no
+    # chunks, and one with packed_len > P_max is flagged and skipped; both must
+    # still come out as zero rows (the output starts as garbage), and every other
+    # request must match the oracle
+    import dataclasses
+    rd = _rd()
+    cfg = dataclasses.replace(workloads.CONFIGS["8b_gqa_b16"], B=6, vocab=50,
+                              ctx=("uniform", 100, 1500))
+    inp = _to_dev(workloads.make_verify_inputs(cfg, device="cpu"))
+    st = _status()
+    pk = rd.rd_pack_beams(inp["beams"], cfg.P_max, dev_status=st)
+    plen = pk["packed_len"].clone()
+    plen[1] = 0
+    plen[3] = cfg.P_max + 5
+    max_ctx = int(inp["ctx_lens"].max())
+    assert rd.rd_tree_attention_workspace_size(cfg.B, cfg.P_max, cfg.Hq, cfg.Hkv, cfg.D,
+                                               max_ctx) > 0      # chunk ranges
+    o = torch.full_like(inp["q"], 7.0)
+    rd.rd_tree_attention(inp["q"], inp["k_draft"], inp["v_draft"], inp["k_cache"],
+                         inp["v_cache"], inp["ctx_offsets"], plen, pk["mask"],
+                         max_ctx=max_ctx, out=o, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() & rd.DEV_BAD_LENGTH
+    got = o.float().cpu().numpy()
+    assert not got[1].any() and not got[3].any()
+    pk_ref = oracle.oracle_pack(inp["beams"].cpu().numpy(), cfg.P_max)
+    plen_ref = pk_ref["packed_len"].copy()
+    plen_ref[1] = 0
+    plen_ref[3] = 0
+    ref = oracle.oracle_tree_attention(bf16_bits(inp["q"]), bf16_bits(inp["k_draft"]),
+                                       bf16_bits(inp["v_draft"]), bf16_bits(inp["k_cache"]),
+                                       bf16_bits(inp["v_cache"]), inp["ctx_offsets"].cpu().numpy(),
+                                       plen_ref, pk_ref["mask"])
+    _close(got, ref, "zero and bad packed lengths")
+
+
 def test_tree_attention_deep_trees_span_draft_chunks():
     # W*L up to 160 packed nodes: the draft segment crosses 64-position chunks
     import dataclasses
