@@ -51,11 +51,13 @@
 #include <mutex>
 #include <type_traits>
 
+#include "attn_common.cuh"
 #include "rd_internal.cuh"
 #include "tc_ptx.cuh"
 
 namespace {
 using namespace rdtc;
+using namespace rdattn;
 
 constexpr int kM = 128;                    // query rows per tile = TMEM lanes
 constexpr int kN = 64;                     // KV positions per chunk
@@ -436,15 +438,6 @@ __device__ __forceinline__ void prefetch_geo(const TcArgs& a, int u)
     asm volatile("prefetch.global.L1 [%0];" ::"l"(p1));
 }
 
-// 16-byte chunk c of row r in a [rows][128 B] tile with the 128-byte swizzle
-__device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
-{
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-}
-
 template <bool F8>
 __device__ __forceinline__ uint32_t pack16(float lo, float hi)
 {
@@ -469,23 +462,6 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w16)
     asm("{\n\t.reg .b16 t;\n\tmov.b16 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
         : "=r"(r) : "h"((unsigned short)w16));
     return r;
-}
-
-// 2^x with the hardware approximation (ex2.approx; 2^-inf = 0)
-__device__ __forceinline__ float fast_exp2(float x)
-{
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// Warp-uniform bounded wait: every lane waits, and the warp fails as one if any
-// lane ran out of budget or saw the abort flag.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          long long budget)
-{
-    const bool ok = mbar_wait(bar, parity, abort, budget);
-    return __all_sync(0xffffffffu, ok);
 }
 
 // The same wait with the waiting loop out of line: for a wait on the softmax
@@ -1489,57 +1465,6 @@ merge_pieces_kernel(const TcArgs a)
 }
 
 // ------------------------------------------------------------------ host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, []() {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-// [rows, heads, D] bf16 -> boxes of 64 positions x 1 head x 64 columns, 128-byte swizzle
-bool make_kv_map(CUtensorMap* map, const void* base, int64_t rows, int heads, int D)
-{
-    auto fn = encode_fn();
-    if (!fn) return false;
-    if (rows < 1) rows = 1;
-    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)heads * D * 2};
-    cuuint32_t box[3] = {64, 1, (cuuint32_t)kN};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
-                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
-// queries [rows, Hq, D] bf16 -> boxes of box_rows positions x G heads x 64 columns,
-// 128-byte swizzle: a box lands as box_rows * G rows of 128 bytes, row p G + g
-bool make_q_map(CUtensorMap* map, const void* base, int64_t rows, int heads, int D, int G,
-                int box_rows)
-{
-    auto fn = encode_fn();
-    if (!fn) return false;
-    if (rows < 1) rows = 1;
-    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)heads * D * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)box_rows};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
-                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 // [rows, heads, D] e4m3 -> boxes of kNc (64) positions x 1 head x D bytes, 128-byte swizzle
 bool make_fp8_map(CUtensorMap* map, const void* base, int64_t rows, int heads, int D)
 {

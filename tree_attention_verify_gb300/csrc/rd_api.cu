@@ -235,12 +235,10 @@ rd_status rd_causal_attention(int B, int Hq, int Hkv, int D, float scale,
     if (B == 0 || max_seqlen == 0 || total_tokens == 0) return RD_OK;
     if (!q || !k || !v || !cu_seqlens || !o) return RD_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return RD_ERR_INVALID_ARG;
-    const rd_attn_plan plan = rd_attn_make_plan(true, B, 1, Hq, Hkv, D, max_seqlen);
     if (scale <= 0.f) scale = 1.0f / sqrtf((float)D);
-    return from_cuda(rd_launch_attention(true, plan, B, 1, Hq, Hkv, D, scale, q, k, v,
-                                         nullptr, nullptr, nullptr, total_tokens, max_seqlen,
-                                         cu_seqlens, nullptr, 0, o, nullptr, dev_status,
-                                         (cudaStream_t)stream));
+    return from_cuda(rd_launch_causal_pair(B, Hq, Hkv, D, scale, q, k, v, cu_seqlens,
+                                           total_tokens, max_seqlen, o, dev_status,
+                                           (cudaStream_t)stream));
 }
 
 rd_status rd_unpack(const void* packed, rd_dtype dt, int B, int P_max, int Dh,

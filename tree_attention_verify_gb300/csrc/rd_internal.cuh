@@ -86,6 +86,12 @@ cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, in
                                 cudaStream_t stream, const rd_paged_kv* paged = nullptr,
                                 const rd_fp8_kv* fp8 = nullptr);
 
+// Causal prefill with paired 128-row query tiles, one CTA per SM (causal_pair.cu).
+cudaError_t rd_launch_causal_pair(int B, int Hq, int Hkv, int D, float scale, const void* q,
+                                  const void* k, const void* v, const int32_t* cu_seqlens,
+                                  int64_t total, int max_len, void* o, int32_t* dev_status,
+                                  cudaStream_t stream);
+
 cudaError_t rd_launch_commit(int B, int W, int L, int P_max, int Hkv, int D, const void* k_new,
                              const void* v_new, const int32_t* unpacker,
                              const int32_t* best_beam, const int32_t* n_accepted, void* k_pool,
