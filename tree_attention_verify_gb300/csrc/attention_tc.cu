@@ -496,6 +496,10 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
     const int warp = tid >> 5, lane = tid & 31;
     volatile int* abort = &bar.abort;
     volatile int no_abort = 0;
+    // the merge launch that follows a chunk-range launch may start now: its CTAs
+    // wait (griddepcontrol.wait) until this grid has completed and its writes are
+    // visible, so only their launch overlaps this kernel's tail
+    if (C::kMaySk && a.sk) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (tid == 0) {
         for (int i = 0; i < C::kStages; ++i) {
@@ -1397,6 +1401,9 @@ merge_pieces_kernel(const TcArgs a)
 {
     constexpr int QC = D / 4;                           // columns per thread (D = 128: 32)
     constexpr int NQ = QC / 4;                          // float4 per thread
+    // launched as a programmatic dependent of the attention grid: wait for it to
+    // complete (and its partials and descriptors to be visible)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int4 dsc = a.sk_desc[blockIdx.x];
     if (dsc.x < 0) return;
     const int bh = a.B * a.Hkv;
@@ -1495,9 +1502,19 @@ cudaError_t launch(int grid, cudaStream_t stream, const TcArgs& a, const CUtenso
     tree_attention_tc_kernel<D, F8, PIPE><<<grid, kThreads, Cf::kSmemBytes, stream>>>(a, m0, m1, m2, m3, m4, m5);
     e = cudaGetLastError();
     if (e != cudaSuccess || !a.sk) return e;
-    // chunk-range division: merge the units that CTA boundaries cut
-    merge_pieces_kernel<D><<<grid, kMergeThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    // chunk-range division: merge the units that CTA boundaries cut, launched as a
+    // programmatic dependent (its launch overlaps the attention kernel's tail)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, merge_pieces_kernel<D>, a);
 }
 
 }  // namespace
