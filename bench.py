@@ -39,7 +39,10 @@ METRIC = "verify_steps_per_s"
 UNIT = "steps/s"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0          # GB300 HBM3e, nominal (context for the measured peak)
-ATTN_SRC = os.path.join(ROOT, "tree_attention_verify_gb300", "csrc", "attention_tc.cu")
+# the sources the tree-attention kernel is compiled from (the ncu traffic figure
+# in profiles/ holds only while their combined hash is the one recorded there)
+ATTN_SRCS = [os.path.join(ROOT, "tree_attention_verify_gb300", "csrc", f)
+             for f in ("attention_tc.cu", "attn_common.cuh", "tc_ptx.cuh")]
 
 
 # ----------------------------------------------------------------------------
@@ -105,9 +108,12 @@ def _peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def _sha256(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+def _sha256(paths):
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def _profile_traffic(workload: str):
@@ -119,7 +125,7 @@ def _profile_traffic(workload: str):
     text = open(path).read()
     m1 = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
     m2 = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
-    if not m1 or not m2 or m2.group(1) != _sha256(ATTN_SRC):
+    if not m1 or not m2 or m2.group(1) != _sha256(ATTN_SRCS):
         return None
     return float(m1.group(1))
 

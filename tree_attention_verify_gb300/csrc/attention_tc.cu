@@ -1,14 +1,14 @@
-// Tree attention (generation phase) and causal prefill (context phase) on the 5th-
-// generation tensor cores: TMA-fed, tcgen05 MMA with TMEM accumulators, persistent.
+// Tree attention (generation phase) on the 5th-generation tensor cores: TMA-fed,
+// tcgen05 MMA with TMEM accumulators, persistent.
 //
 // A single kernel with a topology-aware mask verifies every candidate path at once
-// (speculative-decoding survey page, SpecInfer "Token Tree Verifier"); TensorRT-LLM's
-// attention plugin splits context and generation requests (NVIDIA blog "ReDrafter
-// in TensorRT-LLM", section "Inflight-batching Compatible Engine").
+// (speculative-decoding survey page, SpecInfer "Token Tree Verifier").  The context
+// phase of an in-flight batch (NVIDIA blog "ReDrafter in TensorRT-LLM", section
+// "Inflight-batching Compatible Engine") runs in the paired-tile causal kernel.
 //
 // Work unit = (request b, kv head h, 128-row query tile, KV split).  The G query
 // heads that share kv head h are stacked as rows (row r -> node p = r / G, head
-// h*G + r % G; causal: token t = r / G), so each K/V byte is read once per tile.
+// h*G + r % G), so each K/V byte is read once per tile.
 // A unit walks its KV chunks (64 positions): the context (all visible, the last
 // chunk ragged), then the packed drafts (visible iff the node's ancestor-mask
 // bit is set).  Persistent CTAs, two per SM, take units round-robin in
@@ -25,15 +25,12 @@
 //              O += P V (M=128, N=D, K=64; A = P in TMEM).
 //   warps 6-7  FP8: widen e4m3 chunks into the 16-bit ring; 16-bit paths:
 //              warp 6 loads the query tiles into shared memory (TMA).
-// Tree attention (template flag PIPE) keeps two S tiles in TMEM and issues S of
+// The 16-bit path (template flag PIPE) keeps two S tiles in TMEM and issues S of
 // chunk j+1 before PV of chunk j, so the tensor core computes the next scores
 // while the softmax warps work; its queries sit in shared memory and K and V
-// have separate rings (a K stage frees as soon as S has read it).  Causal
-// prefill and the FP8 path keep one S tile with the queries in TMEM and issue S
-// of a chunk right behind PV of the one before: causal tiles have all 128 rows
-// valid, and reading 32 KB of queries from shared memory for every chunk's S
-// measured slower there, so the issuer copies each unit's shared-memory query
-// tile into TMEM once (tcgen05.cp); the FP8 softmax warps write theirs.
+// have separate rings (a K stage frees as soon as S has read it).  The FP8 path
+// keeps one S tile with the queries in TMEM (written by its softmax warps) and
+// issues S of a chunk right behind PV of the one before.
 // FP8 variant (template flag F8; context K/V stored as e4m3 with per-tensor
 // scales): the producer TMA-loads e4m3 context chunks into an 8-bit ring; warps
 // 6-7 widen them (exactly) into the 16-bit ring the MMA reads, and convert the
@@ -86,13 +83,11 @@ constexpr int kSkMaxB = 480;               // chunk-range division up to this ma
 constexpr uint32_t kSkMinChunks = 8;       // chunks per CTA at least (chunk-range division)
 
 template <int D, bool F8 = false, bool PIPE = false> struct Cfg {
-    // PIPE (16-bit tree attention) pipelines S: two S tiles in tensor memory, so
-    // that S of the next chunk is computed while the softmax warps work on this
-    // one, with the queries in shared memory.  Otherwise (causal prefill, whose
-    // 128-row tiles would re-read the queries from shared memory for every S MMA,
-    // and FP8, whose shared memory holds the 8-bit ring) one S tile and the
-    // queries in tensor memory.
-    static_assert(!(F8 && PIPE), "the FP8 path keeps one S tile");
+    // PIPE (the 16-bit path) pipelines S: two S tiles in tensor memory, so that S
+    // of the next chunk is computed while the softmax warps work on this one,
+    // with the queries in shared memory.  FP8 (whose shared memory holds the
+    // 8-bit ring): one S tile and the queries in tensor memory.
+    static_assert(F8 != PIPE, "every instantiation is the 16-bit pipelined path or the FP8 path");
     static constexpr bool kPipe = PIPE;
     static constexpr bool kMaySk = PIPE || F8;          // tree attention (chunk ranges possible)
     static constexpr int kNc = kN;                      // KV positions per chunk
@@ -101,10 +96,9 @@ template <int D, bool F8 = false, bool PIPE = false> struct Cfg {
     // PIPE: separate K and V rings (a K stage is free once S has read it, so K
     // loads run ahead of the V loads) and the query tile.  Otherwise one ring of
     // K + V stages (16-bit), and for FP8 the 8-bit ring of context chunks.
-    // The 16-bit paths take their query tiles by TMA into shared memory (warp 6);
-    // the causal one then copies each into TMEM (tcgen05.cp) for S's A operand.
-    static constexpr bool kQTma = !F8;
-    static constexpr int kStages = F8 ? 2 : PIPE ? (D == 128 ? 2 : 4) : (D == 128 ? 2 : 5);
+    // The 16-bit path takes its query tiles by TMA into shared memory (warp 6).
+    static constexpr bool kQTma = PIPE;
+    static constexpr int kStages = F8 ? 2 : (D == 128 ? 2 : 4);
     static constexpr int kF8Stages = F8 ? 2 : 0;
     static constexpr int kF8Ring = kF8Stages > 0 ? kF8Stages : 1;   // ring index modulus
     static constexpr int kStageBytes = PIPE ? kKBytes : 2 * kKBytes;
@@ -132,7 +126,6 @@ template <int D, bool F8 = false, bool PIPE = false> struct Cfg {
 };
 
 struct TcArgs {
-    bool causal;
     int B, P_max, Hq, Hkv, G, tiles, mask_words, n_units;   // n_units = B * Hkv * tiles
     // Work division.  Chunk ranges (tree attention, B <= kSkMaxB): the live units'
     // chunks, in request / tile / kv-head order, are one sequence of W chunks,
@@ -200,8 +193,8 @@ struct UnitGeo {
     bool zero_tile;       // tree tile without valid rows: write zeros
     int n_rows;           // valid rows of (b, h)
     int64_t kv_base;      // first row of this request / sequence in the K/V map
-    int C;                // context length (tree) or sequence length (causal)
-    int Pb;               // packed length (tree)
+    int C;                // context length
+    int Pb;               // packed length
     int c_first, n_ctx;   // first context chunk and number of context chunks
     int d_first, n_draft; // first draft chunk and number of draft chunks
     // a piece of a cut unit and its partial slot (2 blockIdx.x, or 2 blockIdx.x
@@ -210,44 +203,33 @@ struct UnitGeo {
     int split;
 };
 
-// Lengths of request (or sequence) b; false (and zero lengths) if they are invalid.
+// Lengths of request b; false (and zero lengths) if they are invalid.
 __device__ __forceinline__ bool req_geo(const TcArgs& a, int b, UnitGeo& g)
 {
     bool bad;
-    if (a.causal) {
-        const int s0 = a.lens[b], s1 = a.lens[b + 1];
-        g.kv_base = s0;
-        g.C = s1 - s0;
-        g.Pb = 0;
-        bad = s0 < 0 || g.C < 0 || g.C > a.max_kv || s1 > a.total_kv;
-        if (bad) g.C = 0;
-        g.n_rows = g.C * a.G;
+    g.Pb = a.lens[b];
+    if (a.block_table != nullptr) {
+        const int c = a.ctx_lens[b];
+        g.kv_base = 0;
+        g.C = c;
+        bad = c < 0 || c > a.max_kv || (long long)c > (long long)a.max_pages * a.page_size ||
+              g.Pb < 0 || g.Pb > a.P_max;
     } else {
-        g.Pb = a.lens[b];
-        if (a.block_table != nullptr) {
-            const int c = a.ctx_lens[b];
-            g.kv_base = 0;
-            g.C = c;
-            bad = c < 0 || c > a.max_kv || (long long)c > (long long)a.max_pages * a.page_size ||
-                  g.Pb < 0 || g.Pb > a.P_max;
-        } else {
-            const int64_t c0 = a.ctx_offsets[b], c1 = a.ctx_offsets[b + 1];
-            g.kv_base = c0;
-            g.C = (int)(c1 - c0);
-            bad = c0 < 0 || c1 < c0 || c1 - c0 > a.max_kv || c1 > a.total_kv || g.Pb < 0 ||
-                  g.Pb > a.P_max;
-        }
-        if (bad) { g.C = 0; g.Pb = 0; }
-        g.n_rows = g.Pb * a.G;
+        const int64_t c0 = a.ctx_offsets[b], c1 = a.ctx_offsets[b + 1];
+        g.kv_base = c0;
+        g.C = (int)(c1 - c0);
+        bad = c0 < 0 || c1 < c0 || c1 - c0 > a.max_kv || c1 > a.total_kv || g.Pb < 0 ||
+              g.Pb > a.P_max;
     }
+    if (bad) { g.C = 0; g.Pb = 0; }
+    g.n_rows = g.Pb * a.G;
     return !bad;
 }
 
 // Whole unit u (round-robin division).  Units run tile-major, then request and
 // kv head: the CTAs take units round-robin, and this order puts the tiles past
 // the valid rows of a tree batch (mostly padding) last instead of interleaving
-// them with the live units, while the long and short causal tiles spread evenly
-// over the CTAs.
+// them with the live units.
 template <int NC>
 __device__ __forceinline__ UnitGeo unit_geo(const TcArgs& a, int u)
 {
@@ -263,13 +245,7 @@ __device__ __forceinline__ UnitGeo unit_geo(const TcArgs& a, int u)
     g.split = 0;
     const bool ok = req_geo(a, g.b, g);
     const int row0 = g.tile * kM;
-    if (a.causal) {
-        if (row0 < g.n_rows) {
-            const int t_max = (min(g.n_rows, row0 + kM) - 1) / a.G;
-            g.n_ctx = t_max / NC + 1;
-            g.live = true;
-        }
-    } else if (row0 >= g.n_rows) {
+    if (row0 >= g.n_rows) {
         g.zero_tile = row0 < a.P_max * a.G;
     } else {
         g.live = true;
@@ -425,15 +401,8 @@ __device__ __forceinline__ bool work_next(const TcArgs& a, const uint32_t* pre, 
 __device__ __forceinline__ void prefetch_geo(const TcArgs& a, int u)
 {
     const int b = (u % (a.B * a.Hkv)) / a.Hkv;
-    const void* p0;
-    const void* p1;
-    if (a.causal) {
-        p0 = a.lens + b;
-        p1 = a.lens + b + 1;
-    } else {
-        p0 = a.lens + b;
-        p1 = a.block_table != nullptr ? (const void*)(a.ctx_lens + b) : (const void*)(a.ctx_offsets + b);
-    }
+    const void* p0 = a.lens + b;
+    const void* p1 = a.block_table != nullptr ? (const void*)(a.ctx_lens + b) : (const void*)(a.ctx_offsets + b);
     asm volatile("prefetch.global.L1 [%0];" ::"l"(p0));
     asm volatile("prefetch.global.L1 [%0];" ::"l"(p1));
 }
@@ -535,7 +504,6 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
     }
     uint32_t* sk_pre = reinterpret_cast<uint32_t*>(smem + C::kSkOff);
     uint32_t* sk_nb = sk_pre + kSkMaxB + 1;
-    // (causal prefill, the one-S-tile 16-bit instantiation, never divides by chunk ranges)
     if constexpr (C::kMaySk) {
         if (a.sk && warp == 0) sk_build<C::kNc>(a, sk_pre, sk_nb, lane);
     }
@@ -773,7 +741,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
         // The next unit's boxes are prefetched into L2 when this unit's are issued.
         auto q_row0 = [&](const UnitGeo& ug) -> int {   // tensor row of the tile's first position
             const int p0 = ug.tile * (kM / a.G);
-            return a.causal ? (int)(ug.kv_base + p0) : ug.b * a.P_max + p0;
+            return ug.b * a.P_max + p0;
         };
         auto paired_of = [&](const UnitGeo& ug) { return ug.n_rows - ug.tile * kM <= 64; };
         // TMA boxes of unit ug: fn(map, smem byte offset, x, y, z)
@@ -794,7 +762,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             const int qr = ug.tile * kM + (paired_of(ug) ? 16 * (m >> 5) + (m & 15) : m);
             if (qr >= ug.n_rows) return nullptr;
             const int qp = qr / a.G;
-            const size_t qrow = a.causal ? (size_t)(ug.kv_base + qp) : (size_t)ug.b * a.P_max + qp;
+            const size_t qrow = (size_t)ug.b * a.P_max + qp;
             return reinterpret_cast<const uint4*>(a.q + (qrow * a.Hq + ug.h * a.G + qr % a.G) * D);
         };
         uint32_t it = 0;
@@ -974,20 +942,6 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                         mma_commit(&bar.pv_done[gg & 1]);
                     }
                 } else {
-                    if constexpr (C::kQTma) {
-                        // the unit's query tile, landed in shared memory, into the Q
-                        // columns: D/16 copies of 128 rows x 16 values, the same K-steps
-                        // as an A operand read from shared memory.  They run in issue
-                        // order after the S MMAs of the unit before (which read the Q
-                        // columns), and the commit behind them frees the shared tile.
-                        tc_fence_after();
-#pragma unroll
-                        for (int ks = 0; ks < D / 16; ++ks) {
-                            const uint32_t a_off = ((ks >> 2) * (kM * 128) + (ks & 3) * 32) >> 4;
-                            tmem_cp_128x256b(tmem + C::kQCol + ks * 8, q_desc + a_off);
-                        }
-                        mma_commit(&bar.q_free);
-                    }
                     for (int j = 0; j < n; ++j) {
                         const uint32_t gg = g + j;
                         const int st = (int)(gg % C::kStages);
@@ -1004,7 +958,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                             mma_tmem_a(tmem + C::kSCol, tmem + C::kQCol + ks * 8, kd + off, idS, ks > 0);
                         }
                         mma_commit(&bar.s_full[0]);
-                        if (!C::kQTma && j == n - 1) mma_commit(&bar.q_free);
+                        if (j == n - 1) mma_commit(&bar.q_free);
                         if (j == 0 && unit_iter > 0 &&
                             !mbar_wait(&bar.o_free, (unit_iter - 1) & 1, abort, kWaitBudget)) {
                             ok = false;
@@ -1055,7 +1009,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             const uint4* src = nullptr;
             if (qv_ok) {
                 const int qp = qr / a.G;
-                const size_t qrow = a.causal ? (size_t)(ug.kv_base + qp) : (size_t)ug.b * a.P_max + qp;
+                const size_t qrow = (size_t)ug.b * a.P_max + qp;
                 src = reinterpret_cast<const uint4*>(a.q + (qrow * a.Hq + ug.h * a.G + qr % a.G) * D);
             }
 #pragma unroll
@@ -1119,7 +1073,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             const int r = paired ? warp * 16 + (lane & 15) : tid;   // row within the tile
             const int row = geo.tile * kM + r;
             const bool valid = row < geo.n_rows;
-            const int qpos = row / a.G;                    // node p (tree) / token t (causal)
+            const int qpos = row / a.G;                    // node p
             // queries not written ahead (the first live unit, or one after a unit
             // that was not live): the S MMAs of the last live unit have completed,
             // as this warp waited for them at that unit's end
@@ -1131,7 +1085,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             // a warp whose rows are all padding reads no scores; it writes zero P
             // rows (the S columns hold scores again every chunk)
             const bool dead = __all_sync(0xffffffffu, !valid);
-            const uint32_t* mrow = (!a.causal && valid)
+            const uint32_t* mrow = valid
                 ? a.mask + ((size_t)geo.b * a.P_max + qpos) * a.mask_words : nullptr;
             // One chunk (global index gg, S in the columns at sc): NCOL = 64 columns
             // per lane, or 32 for a paired lane.  FP8: the commit that completed S_j
@@ -1158,11 +1112,10 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                     for (int c = 0; c < NCOL; ++c) s[c] = -INFINITY;
                 } else if (j < geo.n_ctx) {
                     const int pos0 = (geo.c_first + j) * C::kNc + c0;
-                    const int lim = a.causal ? min(geo.C, qpos + 1) : geo.C;   // visible: pos < lim
-                    if (pos0 + NCOL > lim) {
+                    if (pos0 + NCOL > geo.C) {             // the ragged last context chunk
 #pragma unroll
                         for (int c = 0; c < NCOL; ++c)
-                            if (pos0 + c >= lim) s[c] = -INFINITY;
+                            if (pos0 + c >= geo.C) s[c] = -INFINITY;
                     }
                 } else {
                     const int d0 = (geo.d_first + j - geo.n_ctx) * C::kNc + c0;   // a multiple of 32
@@ -1306,11 +1259,10 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
             const bool split_mode = geo.cut;
             if (!split_mode) {
                 const float inv = (valid && l_row > 0.f) ? a.out_scale / l_row : 0.f;
-                const bool write = valid || (!a.causal && qpos < a.P_max);
+                const bool write = qpos < a.P_max;         // valid rows, and padded rows as zeros
                 uint16_t* dst = nullptr;
                 if (write) {
-                    const size_t orow = a.causal ? (size_t)(geo.kv_base + qpos)
-                                                 : (size_t)geo.b * a.P_max + qpos;
+                    const size_t orow = (size_t)geo.b * a.P_max + qpos;
                     dst = a.o + (orow * a.Hq + hq0 + row % a.G) * D;
                 }
                 // bf16 rows, 32 columns (64 bytes) at a time, each lane its own row
@@ -1333,7 +1285,7 @@ tree_attention_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map
                 }
                 // paired: rows 64-127 of the tile hold no valid row; their padded
                 // outputs are zero (half a row per lane)
-                if (paired && !a.causal) {
+                if (paired) {
                     const int row2 = geo.tile * kM + 64 + r;
                     if (row2 / a.G < a.P_max) {
                         uint4* dst2 = reinterpret_cast<uint4*>(
@@ -1519,23 +1471,22 @@ cudaError_t launch(int grid, cudaStream_t stream, const TcArgs& a, const CUtenso
 
 }  // namespace
 
-rd_attn_plan rd_attn_make_plan(bool causal, int B, int P_max, int Hq, int Hkv, int D,
-                               int max_kv)
+rd_attn_plan rd_attn_make_plan(int B, int P_max, int Hq, int Hkv, int D, int max_kv)
 {
     rd_attn_plan plan;
     const int G = Hq / Hkv;
-    const long rows = causal ? (long)max_kv * G : (long)P_max * G;
+    const long rows = (long)P_max * G;
     plan.tiles = (int)((rows + kM - 1) / kM);
     if (plan.tiles < 1) plan.tiles = 1;
     const long units = (long)B * Hkv * plan.tiles;
     const long ctas = (long)kCtasPerSm * rd_device_sm_count();
-    // chunk ranges for tree attention with fewer units than two per CTA (whole
+    // chunk ranges with fewer units than two per CTA (whole
     // units round-robin leave most CTAs idle or hold the launch on the longest
     // unit), while the request table fits in shared memory and the chunk count
     // in 32 bits; a batch with more units balances well enough whole, and needs
     // no partials, merge or workspace
     const long unit_chunks = ((long)max_kv + kN - 1) / kN + ((long)P_max + kN - 1) / kN;
-    plan.stream_k = !causal && units < 2 * ctas && B <= kSkMaxB && units * unit_chunks < (1L << 31);
+    plan.stream_k = units < 2 * ctas && B <= kSkMaxB && units * unit_chunks < (1L << 31);
     plan.grid = (int)(plan.stream_k ? ctas : std::min(units, ctas));
     if (plan.grid < 1) plan.grid = 1;
     // pieces of cut units: two 128-row fp32 slots (O and (m, l)) per CTA, then
@@ -1547,7 +1498,7 @@ rd_attn_plan rd_attn_make_plan(bool causal, int B, int P_max, int Hq, int Hkv, i
     return plan;
 }
 
-cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, int P_max,
+cudaError_t rd_launch_attention(const rd_attn_plan& plan, int B, int P_max,
                                 int Hq, int Hkv, int D, float scale, const void* q,
                                 const void* k_new, const void* v_new,
                                 const void* k_cache, const void* v_cache,
@@ -1563,7 +1514,6 @@ cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, in
     a.max_pages = paged ? paged->max_pages : 0;
     a.page_size = paged ? paged->page_size : 1;
     a.num_pages = paged ? paged->num_pages : 0;
-    a.causal = causal;
     a.B = B;
     a.P_max = P_max;
     a.Hq = Hq;
@@ -1601,18 +1551,18 @@ cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, in
         a.sk_desc = reinterpret_cast<int4*>(a.ml_part + slot_rows);
     }
     CUtensorMap mkc, mvc, mkd, mvd;
-    const void* kc = causal ? k_new : k_cache;
-    const void* vc = causal ? v_new : v_cache;
+    const void* kc = k_cache;
+    const void* vc = v_cache;
     const int64_t kc_rows = paged ? (int64_t)paged->num_pages * paged->page_size : total_kv;
-    const int64_t kd_rows = causal ? total_kv : (int64_t)B * P_max;
-    const void* kd = causal ? k_new : k_new;
-    const void* vd = causal ? v_new : v_new;
+    const int64_t kd_rows = (int64_t)B * P_max;
+    const void* kd = k_new;
+    const void* vd = v_new;
     if (kc == nullptr || kc_rows == 0) { kc = kd; vc = vd; }
     const int grid = plan.grid;
     a.stall_budget = rd_attention_stall_budget();
     if (fp8 != nullptr) {
         // 8-bit context maps (the drafts are read by the converter warps)
-        if (D != 128 || causal || paged || total_kv < 1 ||
+        if (D != 128 || paged || total_kv < 1 ||
             !make_fp8_map(&mkc, fp8->k_cache, total_kv, Hkv, D) ||
             !make_fp8_map(&mvc, fp8->v_cache, total_kv, Hkv, D))
             return cudaErrorInvalidValue;
@@ -1626,14 +1576,11 @@ cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, in
     // query tiles by TMA when a tile is whole boxes: G a power of two <= 16 (it
     // divides the 16 rows of a paired box and the 128 of a tile)
     CUtensorMap mq128, mq16;
-    const int64_t q_rows = causal ? total_kv : (int64_t)B * P_max;
+    const int64_t q_rows = (int64_t)B * P_max;
     a.q_tma = a.G <= 16 && (a.G & (a.G - 1)) == 0 && (reinterpret_cast<uintptr_t>(q) & 15) == 0 &&
               make_q_map(&mq128, q, q_rows, Hq, D, a.G, kM / a.G) &&
               make_q_map(&mq16, q, q_rows, Hq, D, a.G, 16 / a.G);
     if (!a.q_tma) { mq128 = mkc; mq16 = mkc; }
-    if (causal)
-        return D == 128 ? launch<128, false, false>(grid, stream, a, mkc, mvc, mkd, mvd, mq128, mq16)
-                        : launch<64, false, false>(grid, stream, a, mkc, mvc, mkd, mvd, mq128, mq16);
     return D == 128 ? launch<128, false, true>(grid, stream, a, mkc, mvc, mkd, mvd, mq128, mq16)
                     : launch<64, false, true>(grid, stream, a, mkc, mvc, mkd, mvd, mq128, mq16);
 }

@@ -85,7 +85,7 @@ size_t rd_tree_attention_workspace_size(int B, int P_max, int Hq, int Hkv, int D
                                         int max_ctx)
 {
     if (B <= 0 || P_max < 1 || !attn_shape_ok(Hq, Hkv, D) || max_ctx < 0) return 0;
-    return rd_attn_make_plan(false, B, P_max, Hq, Hkv, D, max_ctx).ws_bytes;
+    return rd_attn_make_plan(B, P_max, Hq, Hkv, D, max_ctx).ws_bytes;
 }
 
 rd_status rd_tree_attention(int B, int P_max, int Hq, int Hkv, int D, float scale,
@@ -108,11 +108,11 @@ rd_status rd_tree_attention(int B, int P_max, int Hq, int Hkv, int D, float scal
     if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
         !aligned16(v_cache) || !aligned16(o) || !aligned16(workspace))
         return RD_ERR_INVALID_ARG;
-    const rd_attn_plan plan = rd_attn_make_plan(false, B, P_max, Hq, Hkv, D, max_ctx);
+    const rd_attn_plan plan = rd_attn_make_plan(B, P_max, Hq, Hkv, D, max_ctx);
     if (plan.ws_bytes > 0 && (!workspace || ws_bytes < plan.ws_bytes))
         return RD_ERR_INVALID_ARG;
     if (scale <= 0.f) scale = 1.0f / sqrtf((float)D);
-    return from_cuda(rd_launch_attention(false, plan, B, P_max, Hq, Hkv, D, scale, q, k_new,
+    return from_cuda(rd_launch_attention(plan, B, P_max, Hq, Hkv, D, scale, q, k_new,
                                          v_new, k_cache, v_cache, ctx_offsets, total_ctx,
                                          max_ctx, packed_len, mask, mask_words, o, workspace,
                                          dev_status, (cudaStream_t)stream));
@@ -141,7 +141,7 @@ rd_status rd_tree_attention_fp8(int B, int P_max, int Hq, int Hkv, int D, float 
     if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
         !aligned16(v_cache) || !aligned16(o) || !aligned16(workspace))
         return RD_ERR_INVALID_ARG;
-    const rd_attn_plan plan = rd_attn_make_plan(false, B, P_max, Hq, Hkv, D, max_ctx);
+    const rd_attn_plan plan = rd_attn_make_plan(B, P_max, Hq, Hkv, D, max_ctx);
     if (plan.ws_bytes > 0 && (!workspace || ws_bytes < plan.ws_bytes))
         return RD_ERR_INVALID_ARG;
     if (scale <= 0.f) scale = 1.0f / sqrtf((float)D);
@@ -150,7 +150,7 @@ rd_status rd_tree_attention_fp8(int B, int P_max, int Hq, int Hkv, int D, float 
     f8.v_cache = v_cache;
     f8.k_scale = k_scale;
     f8.v_scale = v_scale;
-    return from_cuda(rd_launch_attention(false, plan, B, P_max, Hq, Hkv, D, scale, q, k_new,
+    return from_cuda(rd_launch_attention(plan, B, P_max, Hq, Hkv, D, scale, q, k_new,
                                          v_new, nullptr, nullptr, ctx_offsets, total_ctx,
                                          max_ctx, packed_len, mask, mask_words, o, workspace,
                                          dev_status, (cudaStream_t)stream, nullptr, &f8));
@@ -180,7 +180,7 @@ rd_status rd_tree_attention_paged(int B, int P_max, int Hq, int Hkv, int D, floa
     if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) ||
         !aligned16(v_pool) || !aligned16(o) || !aligned16(workspace))
         return RD_ERR_INVALID_ARG;
-    const rd_attn_plan plan = rd_attn_make_plan(false, B, P_max, Hq, Hkv, D, max_ctx);
+    const rd_attn_plan plan = rd_attn_make_plan(B, P_max, Hq, Hkv, D, max_ctx);
     if (plan.ws_bytes > 0 && (!workspace || ws_bytes < plan.ws_bytes))
         return RD_ERR_INVALID_ARG;
     if (scale <= 0.f) scale = 1.0f / sqrtf((float)D);
@@ -190,7 +190,7 @@ rd_status rd_tree_attention_paged(int B, int P_max, int Hq, int Hkv, int D, floa
     pg.max_pages = max_pages;
     pg.page_size = page_size;
     pg.num_pages = num_pages;
-    return from_cuda(rd_launch_attention(false, plan, B, P_max, Hq, Hkv, D, scale, q, k_new,
+    return from_cuda(rd_launch_attention(plan, B, P_max, Hq, Hkv, D, scale, q, k_new,
                                          v_new, num_pages > 0 ? k_pool : nullptr,
                                          num_pages > 0 ? v_pool : nullptr, nullptr, 0, max_ctx,
                                          packed_len, mask, mask_words, o, workspace,

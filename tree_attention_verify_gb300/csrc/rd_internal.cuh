@@ -57,7 +57,7 @@ cudaError_t rd_launch_sample_accept(const void* target, const void* draft, int B
                                     int32_t* n_accepted, int32_t* out_tokens,
                                     int32_t* dev_status, cudaStream_t stream);
 
-// Attention (tree and causal modes share one kernel family).
+// Tree attention (attention_tc.cu): the 16-bit, paged and FP8 variants.
 struct rd_attn_plan {
     int tiles;         // row tiles per (request, kv head)
     bool stream_k;     // chunk-range division (tree attention), else whole units round-robin
@@ -74,9 +74,8 @@ struct rd_fp8_kv {
     const void* v_cache;
     float k_scale, v_scale;
 };
-rd_attn_plan rd_attn_make_plan(bool causal, int B, int P_max, int Hq, int Hkv, int D,
-                               int max_kv);
-cudaError_t rd_launch_attention(bool causal, const rd_attn_plan& plan, int B, int P_max,
+rd_attn_plan rd_attn_make_plan(int B, int P_max, int Hq, int Hkv, int D, int max_kv);
+cudaError_t rd_launch_attention(const rd_attn_plan& plan, int B, int P_max,
                                 int Hq, int Hkv, int D, float scale, const void* q,
                                 const void* k_new, const void* v_new,
                                 const void* k_cache, const void* v_cache,
