@@ -653,7 +653,10 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "next_rows": next_rows,
-            "gpu_launches": 4 * K,
+            # per step: pack, attention (+ the merge launch when the batch takes
+            # chunk ranges), greedy accept, unpack
+            "gpu_launches": (1 + (2 if rd.rd_tree_attention_workspace_size(
+                cfg.B, cfg.P_max, cfg.Hq, cfg.Hkv, cfg.D, max_ctx, dev) > 0 else 1) + 1 + 1) * K,
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)
