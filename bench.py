@@ -436,6 +436,7 @@ def measure_mixed(dev) -> dict:
     import tree_attention_verify_gb300 as rd
     from tree_attention_verify_gb300.step import VerifyStep
     peak_tf, _ = _peak_tflops()
+    peak_gbs, _ = _peak_hbm()
     out = {}
     for split in ("mixed", "all_ctx", "all_gen"):
         m = workloads.make_mixed_inputs(split, device=dev)
@@ -459,10 +460,19 @@ def measure_mixed(dev) -> dict:
                                                      workspace=wsc, dev_status=st))
             Hq, D = c["q"].shape[1], c["q"].shape[2]
             flops = float(sum(4.0 * Hq * D * t * (t + 1) / 2 for t in c["seq_lens"]))
+            # algorithmic bytes: q, k, v read once, o written once
+            nbytes = float(2 * c["q"].numel() + c["k"].numel() + c["v"].numel()) * 2.0
             us = _time_us(causal)
+            # the binding roof is the one with the longer minimum time
+            hbm_bound = nbytes / (peak_gbs * 1e3) >= flops / (peak_tf * 1e6)
             row["rd_causal_attention"] = {"us": us, "tflops": flops / us / 1e6,
-                                          "frac": flops / us / 1e6 / peak_tf,
-                                          "bound": "tensor"}
+                                          "tensor_frac": flops / us / 1e6 / peak_tf,
+                                          "gbs": nbytes / us / 1e3,
+                                          "hbm_frac": nbytes / us / 1e3 / peak_gbs,
+                                          "algorithmic_bytes": nbytes,
+                                          "bound": "hbm" if hbm_bound else "tensor",
+                                          "frac": (nbytes / us / 1e3 / peak_gbs) if hbm_bound
+                                          else flops / us / 1e6 / peak_tf}
         if n_gen:
             gc = g["cfg"]
             step = VerifyStep(gc.B, gc.W, gc.L, gc.Hq, gc.Hkv, gc.D, gc.vocab, gc.Dh,
