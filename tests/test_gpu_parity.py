@@ -389,6 +389,37 @@ def test_causal_attention(lens, Hq, Hkv, D):
     _close(o.float().cpu().numpy(), ref, "causal")
 
 
+def test_causal_attention_many_units_sampled():
+    """48 sequences of 1-1024 tokens on 8B shapes (32 query / 8 kv heads x 128):
+    about 40 units per CTA, whole and partial 128-row tiles, pairs with one or
+    two live tiles, output tiles both by TMA stores and by row stores.  Sampled
+    (sequence, kv head) slices are compared with the oracle run on that slice
+    alone (causal attention is independent per sequence and kv head)."""
+    rd = _rd()
+    rng = np.random.default_rng(2026)
+    lens = rng.integers(1, 1025, size=48).astype(np.int64)
+    lens[:4] = (1024, 1, 257, 32)
+    Hq, Hkv, D = 32, 8, 128
+    G = Hq // Hkv
+    gen = torch.Generator(device="cpu").manual_seed(7)
+    inp = workloads.make_context_inputs(len(lens), 0, Hq, Hkv, D, 100, gen, "cpu", lens=lens)
+    st = _status()
+    o = rd.rd_causal_attention(inp["q"].to(DEV), inp["k"].to(DEV), inp["v"].to(DEV),
+                               inp["cu_seqlens"].to(DEV), max_seqlen=int(lens.max()), dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    o = o.float().cpu().numpy()
+    cu = inp["cu_seqlens"].numpy()
+    q16, k16, v16 = bf16_bits(inp["q"]), bf16_bits(inp["k"]), bf16_bits(inp["v"])
+    samples = [(0, 0), (1, 7), (2, 3), (3, 5)] + [(int(rng.integers(48)), int(rng.integers(Hkv)))
+                                                  for _ in range(6)]
+    for b, h in samples:
+        s0, s1 = int(cu[b]), int(cu[b + 1])
+        ref = oracle.oracle_causal_attention(q16[s0:s1, h * G:(h + 1) * G], k16[s0:s1, h:h + 1],
+                                             v16[s0:s1, h:h + 1], np.array([0, s1 - s0], np.int32))
+        _close(o[s0:s1, h * G:(h + 1) * G], ref, f"causal b={b} h={h}")
+
+
 # ------------------------------------------------------------------------------
 # the whole verification step, and the in-flight mixed batch
 # ------------------------------------------------------------------------------
