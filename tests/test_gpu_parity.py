@@ -420,6 +420,30 @@ def test_causal_attention_many_units_sampled():
         _close(o[s0:s1, h * G:(h + 1) * G], ref, f"causal b={b} h={h}")
 
 
+@pytest.mark.parametrize("lens,Hq,Hkv,D", [([3000, 1500, 77], 32, 8, 128), ([2500, 640], 8, 8, 64)])
+def test_causal_attention_long_sampled(lens, Hq, Hkv, D):
+    """Long sequences: up to 47 chunks per unit, the K/V ring wrapping many times
+    within a unit.  Sampled (sequence, kv head) slices against the oracle."""
+    rd = _rd()
+    G = Hq // Hkv
+    gen = torch.Generator(device="cpu").manual_seed(len(lens) * 1000 + D)
+    inp = workloads.make_context_inputs(len(lens), 0, Hq, Hkv, D, 100, gen, "cpu",
+                                        lens=np.array(lens, np.int64))
+    st = _status()
+    o = rd.rd_causal_attention(inp["q"].to(DEV), inp["k"].to(DEV), inp["v"].to(DEV),
+                               inp["cu_seqlens"].to(DEV), max_seqlen=max(lens), dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    o = o.float().cpu().numpy()
+    cu = inp["cu_seqlens"].numpy()
+    q16, k16, v16 = bf16_bits(inp["q"]), bf16_bits(inp["k"]), bf16_bits(inp["v"])
+    for b, h in [(0, 0), (0, Hkv - 1), (1, Hkv // 2), (len(lens) - 1, 1)]:
+        s0, s1 = int(cu[b]), int(cu[b + 1])
+        ref = oracle.oracle_causal_attention(q16[s0:s1, h * G:(h + 1) * G], k16[s0:s1, h:h + 1],
+                                             v16[s0:s1, h:h + 1], np.array([0, s1 - s0], np.int32))
+        _close(o[s0:s1, h * G:(h + 1) * G], ref, f"causal long b={b} h={h}")
+
+
 # ------------------------------------------------------------------------------
 # the whole verification step, and the in-flight mixed batch
 # ------------------------------------------------------------------------------
