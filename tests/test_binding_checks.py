@@ -60,3 +60,23 @@ def test_accept_shapes_reject_mismatched_outputs(key, bad):
     del out[key]
     with pytest.raises(TypeError):
         rd._accept_shapes(*_accept_args(), out=out)
+
+
+def test_out_helper_rejects_wrong_shape_and_dtype():
+    """Caller-supplied outputs of every other entry point go through _out: the
+    shape and dtype are checked before anything is launched."""
+    import tree_attention_verify_gb300 as rd
+    like = torch.zeros(3, 4, 8, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        rd._out(torch.zeros(3, 4, 7, dtype=torch.bfloat16), "out", like.shape, torch.bfloat16, like)
+    with pytest.raises(TypeError):
+        rd._out(torch.zeros(3, 4, 8, dtype=torch.float32), "out", like.shape, torch.bfloat16, like)
+    with pytest.raises(TypeError):
+        rd._out([1, 2], "out", like.shape, torch.bfloat16, like)
+    # a dict of outputs: a wrong entry is rejected, a missing one is allocated
+    shapes = dict(a=(2, 3), b=(2,))
+    dtypes = dict(a=torch.int32, b=torch.int32)
+    with pytest.raises(ValueError):
+        rd._out_dict(dict(a=torch.zeros(2, 4, dtype=torch.int32)), shapes, dtypes, like)
+    got = rd._out_dict(None, shapes, dtypes, like)
+    assert tuple(got["a"].shape) == (2, 3) and tuple(got["b"].shape) == (2,)

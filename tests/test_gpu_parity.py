@@ -444,6 +444,29 @@ def test_causal_attention_long_sampled(lens, Hq, Hkv, D):
         _close(o[s0:s1, h * G:(h + 1) * G], ref, f"causal long b={b} h={h}")
 
 
+def test_wrong_out_buffers_are_rejected_before_launch():
+    """A caller-supplied output of the wrong shape or dtype raises before any
+    kernel runs (it would otherwise be written out of bounds)."""
+    rd = _rd()
+    q = torch.zeros(64, 8, 128, dtype=torch.bfloat16, device=DEV)
+    k = torch.zeros(64, 2, 128, dtype=torch.bfloat16, device=DEV)
+    cu = torch.tensor([0, 64], dtype=torch.int32, device=DEV)
+    with pytest.raises(ValueError):
+        rd.rd_causal_attention(q, k, k, cu, max_seqlen=64, out=torch.empty(63, 8, 128, dtype=torch.bfloat16,
+                                                                            device=DEV))
+    with pytest.raises(TypeError):
+        rd.rd_causal_attention(q, k, k, cu, max_seqlen=64, out=torch.empty(64, 8, 128, dtype=torch.float16,
+                                                                            device=DEV))
+    packed = torch.zeros(2, 6, 16, dtype=torch.bfloat16, device=DEV)
+    unp = torch.zeros(2, 2, 3, dtype=torch.int32, device=DEV)
+    with pytest.raises(ValueError):
+        rd.rd_unpack(packed, unp, out=torch.empty(2, 2, 3, 15, dtype=torch.bfloat16, device=DEV))
+    beams = torch.zeros(2, 2, 3, dtype=torch.int32, device=DEV)
+    with pytest.raises(ValueError):
+        rd.rd_pack_beams(beams, 6, out=dict(tokens=torch.empty(2, 5, dtype=torch.int32, device=DEV)))
+    torch.cuda.synchronize()
+
+
 # ------------------------------------------------------------------------------
 # the whole verification step, and the in-flight mixed batch
 # ------------------------------------------------------------------------------

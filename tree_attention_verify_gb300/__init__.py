@@ -128,6 +128,29 @@ def _empty(shape, dtype, like: torch.Tensor):
     return torch.empty(shape, dtype=dtype, device=like.device)
 
 
+def _out(t, name: str, shape, dtype, like: torch.Tensor) -> torch.Tensor:
+    """A caller-supplied output: allocated if None, else checked (shape, dtype,
+    device, contiguity) before anything is launched, so that a kernel never
+    writes outside it."""
+    if t is None:
+        return _empty(shape, dtype, like)
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must be {tuple(shape)}, got {tuple(t.shape)}")
+    _need(t, name, dtype, like.device)
+    return t
+
+
+def _out_dict(out, shapes: dict, dtypes: dict, like: torch.Tensor) -> dict:
+    if out is None:
+        return {k: _empty(shapes[k], dtypes[k], like) for k in shapes}
+    if not isinstance(out, dict):
+        raise TypeError("out must be a dict of tensors")
+    return {k: _out(out.get(k), f"out[{k!r}]", shapes[k], dtypes[k], like) if k in out
+            else _empty(shapes[k], dtypes[k], like) for k in shapes}
+
+
 _ACCEPT_OUTS = ("argmax", "accept_len", "best_beam", "n_accepted", "out_tokens")
 
 
@@ -174,13 +197,11 @@ def rd_pack_beams(beams: torch.Tensor, P_cap: Optional[int] = None, *, out: Opti
     B, W, L = beams.shape
     P_cap = W * L if P_cap is None else int(P_cap)
     NW = (P_cap + 31) // 32
-    if out is None:
-        out = dict(tokens=_empty((B, P_cap), torch.int32, beams),
-                   packer=_empty((B, P_cap), torch.int32, beams),
-                   unpacker=_empty((B, W, L), torch.int32, beams),
-                   mask=_empty((B, P_cap, NW), torch.int32, beams),   # uint32 bit rows
-                   depth=_empty((B, P_cap), torch.int32, beams),
-                   packed_len=_empty((B,), torch.int32, beams))
+    # mask: uint32 bit rows held as int32
+    out = _out_dict(out, dict(tokens=(B, P_cap), packer=(B, P_cap), unpacker=(B, W, L),
+                              mask=(B, P_cap, NW), depth=(B, P_cap), packed_len=(B,)),
+                    dict.fromkeys(("tokens", "packer", "unpacker", "mask", "depth", "packed_len"),
+                                  torch.int32), beams)
     _run("rd_pack_beams", beams,
         _ptr(beams), B, W, L, P_cap, _ptr(out["tokens"]), _ptr(out["packer"]),
         _ptr(out["unpacker"]), _ptr(out["mask"]), _ptr(out.get("depth")),
@@ -224,8 +245,7 @@ def rd_tree_attention(q, k_new, v_new, k_cache, v_cache, ctx_offsets, packed_len
         raise ValueError("k_cache/v_cache must be [total_ctx, Hkv, D]")
     if ctx_offsets.numel() != B + 1 or packed_len.numel() != B or mask.shape[:2] != (B, P):
         raise ValueError("ctx_offsets/packed_len/mask shapes do not match q")
-    if out is None:
-        out = torch.empty_like(q)
+    out = _out(out, "out", q.shape, torch.bfloat16, q)
     ws_need = rd_tree_attention_workspace_size(B, P, Hq, Hkv, D, max_ctx, q.device)
     if ws_need and workspace is None:
         workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
@@ -265,8 +285,7 @@ def rd_tree_attention_fp8(q, k_new, v_new, k_cache, v_cache, k_scale: float, v_s
         raise ValueError("k_cache/v_cache must be [total_ctx, Hkv, D]")
     if ctx_offsets.numel() != B + 1 or packed_len.numel() != B or mask.shape[:2] != (B, P):
         raise ValueError("ctx_offsets/packed_len/mask shapes do not match q")
-    if out is None:
-        out = torch.empty_like(q)
+    out = _out(out, "out", q.shape, torch.bfloat16, q)
     ws_need = rd_tree_attention_workspace_size(B, P, Hq, Hkv, D, max_ctx, q.device)
     if ws_need and workspace is None:
         workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
@@ -303,8 +322,7 @@ def rd_tree_attention_paged(q, k_new, v_new, k_pool, v_pool, block_table, ctx_le
         raise ValueError("k_pool/v_pool must be [num_pages, page_size, Hkv, D]")
     if block_table.shape[0] != B or ctx_lens.numel() != B or packed_len.numel() != B:
         raise ValueError("block_table/ctx_lens/packed_len do not match the batch")
-    if out is None:
-        out = torch.empty_like(q)
+    out = _out(out, "out", q.shape, torch.bfloat16, q)
     ws_need = rd_tree_attention_workspace_size(B, P, Hq, Hkv, D, max_ctx, q.device)
     if ws_need and workspace is None:
         workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
@@ -352,8 +370,7 @@ def rd_causal_attention(q, k, v, cu_seqlens, *, max_seqlen: int, scale: float = 
     T, Hq, D = q.shape
     if k.shape[0] != T or v.shape != k.shape or k.shape[2] != D:
         raise ValueError("k/v must be [T, Hkv, D] with the rows of q")
-    if out is None:
-        out = torch.empty_like(q)
+    out = _out(out, "out", q.shape, torch.bfloat16, q)
     _run("rd_causal_attention", q,
         cu_seqlens.numel() - 1, Hq, k.shape[1], D, float(scale), _ptr(q), _ptr(k), _ptr(v),
         _ptr(cu_seqlens), T, int(max_seqlen), _ptr(out), _ptr(dev_status), stream=stream)
@@ -371,8 +388,7 @@ def rd_unpack(packed: torch.Tensor, unpacker: torch.Tensor, *, out=None, dev_sta
     _, W, L = unpacker.shape
     if unpacker.shape[0] != B:
         raise ValueError("unpacker batch does not match packed")
-    if out is None:
-        out = _empty((B, W, L, Dh), packed.dtype, packed)
+    out = _out(out, "out", (B, W, L, Dh), packed.dtype, packed)
     _run("rd_unpack", packed, _ptr(packed), _DTYPES[packed.dtype], B, P, Dh, _ptr(unpacker), W,
          L, _ptr(out), _ptr(dev_status), stream=stream)
     return out
@@ -430,11 +446,9 @@ def rd_sample_accept(target_logits, draft_logits, temperature: float, beams, pac
         raise ValueError("draft_logits / packer shapes do not match target_logits")
     if u_accept.shape != (B, P) or u_sample.shape != (B, V):
         raise ValueError("u_accept must be [B, P_max] and u_sample [B, V]")
-    if out is None:
-        out = dict(accept_len=_empty((B, W), torch.int32, target_logits),
-                   best_beam=_empty((B,), torch.int32, target_logits),
-                   n_accepted=_empty((B,), torch.int32, target_logits),
-                   out_tokens=_empty((B, L), torch.int32, target_logits))
+    out = _out_dict(out, dict(accept_len=(B, W), best_beam=(B,), n_accepted=(B,), out_tokens=(B, L)),
+                    dict.fromkeys(("accept_len", "best_beam", "n_accepted", "out_tokens"), torch.int32),
+                    target_logits)
     _run("rd_sample_accept", target_logits,
         _ptr(target_logits), _ptr(draft_logits), B, P, V, float(temperature), _ptr(beams),
         _ptr(packer), _ptr(unpacker), _ptr(packed_len), W, L, _ptr(u_accept), _ptr(u_sample),
@@ -477,10 +491,8 @@ def rd_beam_search_step(logits, scores_in, beams_in, *, out=None, dev_status=Non
     _need(beams_in, "beams_in", torch.int32, logits.device, ndim=3)
     B, W, V = logits.shape
     t = beams_in.shape[2]
-    if out is None:
-        out = dict(beams=_empty((B, W, t + 1), torch.int32, logits),
-                   scores=_empty((B, W), torch.float32, logits),
-                   parent=_empty((B, W), torch.int32, logits))
+    out = _out_dict(out, dict(beams=(B, W, t + 1), scores=(B, W), parent=(B, W)),
+                    dict(beams=torch.int32, scores=torch.float32, parent=torch.int32), logits)
     _run("rd_beam_search_step", logits,
         _ptr(logits), _ptr(scores_in), _ptr(beams_in) if t > 0 else None, B, W, V, t,
         _ptr(out["beams"]), _ptr(out["scores"]), _ptr(out["parent"]), _ptr(dev_status),
