@@ -373,7 +373,8 @@ def test_tree_attention_13b_full_size_sampled():
 # ------------------------------------------------------------------------------
 @pytest.mark.parametrize("lens,Hq,Hkv,D", [([512, 512, 512], 32, 8, 128), ([1, 37, 200, 64], 8, 2, 64),
                                            ([130], 4, 4, 128), ([300, 17], 6, 2, 128),
-                                           ([777, 5, 256], 16, 1, 64), ([1000, 0, 129], 8, 1, 128)])
+                                           ([777, 5, 256], 16, 1, 64), ([1000, 0, 129], 8, 1, 128),
+                                           ([200, 9], 128, 1, 64), ([150, 301], 4, 2, 128)])
 def test_causal_attention(lens, Hq, Hkv, D):
     rd = _rd()
     gen = torch.Generator(device="cpu").manual_seed(sum(lens))
