@@ -8,15 +8,24 @@
 // candidates (best first; equal scores go to the lower w*V + v) become the new
 // beams.  A beam whose score is -inf (not live yet) contributes no candidate.
 //
-// One thread-block cluster of up to four CTAs per request; CTA r takes beam
-// rows r, r + 4, ... (clusters of four with two rows per CTA measured faster
-// than one CTA per row at W = 8).  For each of its rows a CTA streams the row
-// with 16-byte loads for the running (max, sum of exponentials) and the
-// candidates, and selects the row's W best tokens (higher value first, lower
-// token on ties), which are also its best candidates since the row's score
-// offset scores_in[w] - lse[w] is common to them.  Rank 0 of the cluster reads
-// every row's log-sum-exp and W candidates from distributed shared memory and
-// picks the request's W best.  No CTA waits for another outside its cluster.
+// One thread-block cluster of C CTAs per request; CTA r takes beam rows r,
+// r + C, ....  C = min(W, 8) while the grid fits one wave of two CTAs per SM,
+// else min(W, 4) (measured at W = 8: one row per CTA is faster while every CTA
+// has its own slot; at 64 requests, two rows per CTA in one wave beat two
+// waves of one).  For each of its rows a CTA finds the row's
+// log-sum-exp and its W best tokens (higher value first, lower token on ties),
+// which are also its best candidates since the row's score offset
+// scores_in[w] - lse[w] is common to them.  A row of up to kRegQ x 8 x kThreads
+// tokens is read once, with 16-byte loads, into registers: its maximum by packed
+// bf16 max, then the sum of exponentials without rescaling, then the tokens at
+// or above a threshold (below) from the same registers.  Longer or unaligned
+// rows are streamed twice with a running (max, sum).  Selections are by place:
+// a candidate's place is the number of candidates ordered before it, counted by
+// its own thread, so every candidate is placed at once with no rounds of
+// reductions.  Every CTA writes its rows' log-sum-exp and W best into rank 0's
+// shared memory and leaves after one cluster barrier; rank 0 places the W x W
+// candidates and writes the new beams, whose prefixes and scores it staged at
+// start.  No CTA waits for another outside its cluster.
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
@@ -29,8 +38,12 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kNoIndex = 0x7fffffff;
-constexpr int kMaxCluster = 4;           // CTAs per request
-constexpr int kCap = 1024;                 // candidate slots per row
+constexpr int kMaxCluster = 8;           // CTAs per request, at most
+constexpr int kCtasPerSm = 2;            // resident CTAs per SM (64 registers x 512 threads)
+constexpr int kCap = 1024;                 // candidate slots per row (and W x W merge slots)
+constexpr int kRegQ = 8;                   // 16-byte words per thread held in registers
+constexpr uint32_t kNegInf2 = 0xff80ff80u; // two bf16 -inf
+constexpr int kPrefixCap = 512;            // beam prefixes staged in shared memory up to W t
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -38,6 +51,30 @@ constexpr float kLn2 = 0.6931471805599453f;
 __device__ __forceinline__ bool before(float s1, int i1, float s2, int i2)
 {
     return s1 > s2 || (s1 == s2 && i1 < i2);
+}
+
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b)   // per-half bf16 max
+{
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+__device__ __forceinline__ float lo_bf16(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_bf16(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ float ex2(float x)      // 2^x; x <= 0 here, -inf gives 0
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// the larger of the two bf16 values of every word of a 16-byte group, as fp32
+__device__ __forceinline__ float group_max(const uint4& x)
+{
+    const uint32_t m = bmax2(bmax2(x.x, x.y), bmax2(x.z, x.w));
+    return fmaxf(lo_bf16(m), hi_bf16(m));
 }
 
 template <int W>
@@ -48,14 +85,16 @@ struct RowOut {
 };
 
 template <int W>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
 beam_step_kernel(const uint16_t* __restrict__ logits, const float* __restrict__ scores_in,
                  const int32_t* __restrict__ beams_in, int V, int t,
                  int32_t* __restrict__ beams_out, float* __restrict__ scores_out,
                  int32_t* __restrict__ parent, int32_t* dev_status)
 {
-    constexpr int kRowsPerCta = (W + kMaxCluster - 1) / kMaxCluster;
-    __shared__ RowOut<W> s_row[kRowsPerCta];
+    __shared__ RowOut<W> s_row[W];            // this CTA's rows (ceil(W / C) of them)
+    __shared__ RowOut<W> s_all[W];            // rank 0: every row of the request
+    __shared__ float s_sc[W];                 // rank 0: scores_in of the request
+    __shared__ int s_bin[kPrefixCap];         // rank 0: beams_in of the request (W t <= cap)
     __shared__ float2 s_red[kWarps];
     __shared__ float s_rs[kWarps];
     __shared__ int s_ri[kWarps];
@@ -70,6 +109,17 @@ beam_step_kernel(const uint16_t* __restrict__ logits, const float* __restrict__ 
     const int rank = (int)cl.block_rank();
     const int b = blockIdx.x / C;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    static_assert(W * W <= kCap, "merge slots");
+
+    // The CTAs write their rows into rank 0's shared memory once every CTA of the
+    // cluster has started: arrive now, wait just before those writes.
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    const bool stage_prefix = W * t <= kPrefixCap;
+    if (rank == 0) {                           // what the merge reads, early
+        if (tid < W) s_sc[tid] = scores_in[(size_t)b * W + tid];
+        if (stage_prefix)
+            for (int e = tid; e < W * t; e += kThreads) s_bin[e] = beams_in[(size_t)b * W * t + e];
+    }
 
     // W rounds of a CTA-wide (best score, lowest index) selection over the
     // threads' sorted lists ls/li; the winners land in s_win / s_wi
@@ -109,22 +159,23 @@ beam_step_kernel(const uint16_t* __restrict__ logits, const float* __restrict__ 
     };
 
     // ---- this CTA's rows: one pass each --------------------------------------
-    for (int k = 0; k < kRowsPerCta; ++k) {
+    const int rows = (W + C - 1) / C;
+    const int n4 = V / 8;
+    for (int k = 0; k < rows; ++k) {
         const int w = rank + k * C;
         RowOut<W>& out = s_row[k];
-        const bool live = w < W && scores_in[(size_t)b * W + w] != -INFINITY;
-        if (!live) {
+        if (w >= W || scores_in[(size_t)b * W + w] == -INFINITY) {   // no candidates
             if (tid == 0) out.lse = -INFINITY;
             continue;
         }
         const uint16_t* row = logits + ((size_t)b * W + w) * V;
         const bool vec = (V % 8 == 0) && (reinterpret_cast<uintptr_t>(row) % 16 == 0);
+        const uint4* r4 = reinterpret_cast<const uint4*>(row);
+        const bool in_regs = vec && n4 <= kRegQ * kThreads;
         // visit every token of the row: f(logit, token), four 16-byte loads in
         // flight per thread before any of them is used
         auto for_row = [&](auto&& f) {
             if (vec) {
-                const uint4* r4 = reinterpret_cast<const uint4*>(row);
-                const int n4 = V / 8;
                 for (int base = tid; base < n4; base += 4 * kThreads) {
                     uint4 x[4];
 #pragma unroll
@@ -139,8 +190,8 @@ beam_step_kernel(const uint16_t* __restrict__ logits, const float* __restrict__ 
                         const uint32_t xw[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            f(__uint_as_float(xw[e] << 16), i * 8 + 2 * e);
-                            f(__uint_as_float(xw[e] & 0xffff0000u), i * 8 + 2 * e + 1);
+                            f(lo_bf16(xw[e]), i * 8 + 2 * e);
+                            f(hi_bf16(xw[e]), i * 8 + 2 * e + 1);
                         }
                     }
                 }
@@ -149,41 +200,58 @@ beam_step_kernel(const uint16_t* __restrict__ logits, const float* __restrict__ 
                     f(__uint_as_float((uint32_t)__ldg(row + v) << 16), v);
             }
         };
-        // ---- pass 1: log-sum-exp and every thread's best token ----------------
-        float m = -INFINITY, sum = 0.f;          // log2 units
-        float bv = -INFINITY;
-        int bi = kNoIndex;
-        for_row([&](float x, int v) {
-            const float y = x * kLog2e;
-            if (y > m) { sum = (m == -INFINITY) ? 0.f : sum * exp2f(m - y); m = y; }
-            if (y != -INFINITY) sum += exp2f(y - m);
-            if (before(x, v, bv, bi)) { bv = x; bi = v; }
-        });
+        // ---- pass 1: this thread's maximum and sum of exponentials (log2 units)
+        float m = -INFINITY, sum = 0.f, tmax = -INFINITY;
+        uint4 x[kRegQ];                            // the held row (in_regs)
+        if (in_regs) {
+#pragma unroll
+            for (int q = 0; q < kRegQ; ++q) {
+                const int i = tid + q * kThreads;
+                x[q] = i < n4 ? __ldg(r4 + i) : make_uint4(kNegInf2, kNegInf2, kNegInf2, kNegInf2);
+            }
+#pragma unroll
+            for (int q = 0; q < kRegQ; ++q) tmax = fmaxf(tmax, group_max(x[q]));
+            if (tmax != -INFINITY) {
+                m = tmax * kLog2e;
+#pragma unroll
+                for (int q = 0; q < kRegQ; ++q) {
+                    if (tid + q * kThreads < n4) {
+                        const uint32_t xw[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            sum += ex2(fmaf(lo_bf16(xw[e]), kLog2e, -m)) +
+                                   ex2(fmaf(hi_bf16(xw[e]), kLog2e, -m));
+                    }
+                }
+            }
+        } else {
+            for_row([&](float xv, int) {
+                const float y = xv * kLog2e;
+                if (y > m) { sum = (m == -INFINITY) ? 0.f : sum * ex2(m - y); m = y; }
+                if (y != -INFINITY) sum += ex2(y - m);
+                tmax = fmaxf(tmax, xv);
+            });
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             const float om = __shfl_xor_sync(0xffffffffu, m, o);
             const float os = __shfl_xor_sync(0xffffffffu, sum, o);
             const float nm = fmaxf(m, om);
-            sum = (nm == -INFINITY) ? 0.f : sum * exp2f(m - nm) + os * exp2f(om - nm);
+            sum = (nm == -INFINITY) ? 0.f : sum * ex2(m - nm) + os * ex2(om - nm);
             m = nm;
         }
-        // a threshold: the W-th best of a warp's 32 thread maxima.  At least W
+        // a threshold: the W-th largest of a warp's 32 thread maxima.  At least W
         // tokens of the row reach it, so every token of the row's top W does too
         float tw = -INFINITY;
         {
-            float cv = bv;
-            int ci = bi;
+            float cv = tmax;
             for (int r = 0; r < W; ++r) {
-                float ws = cv;
-                int wi = ci;
+                float wm = cv;
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const float os = __shfl_xor_sync(0xffffffffu, ws, o);
-                    const int oi = __shfl_xor_sync(0xffffffffu, wi, o);
-                    if (before(os, oi, ws, wi)) { ws = os; wi = oi; }
-                }
-                if (r == W - 1) tw = (wi == kNoIndex) ? -INFINITY : ws;
-                if (ci != kNoIndex && ci == wi) { cv = -INFINITY; ci = kNoIndex; }
+                for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+                tw = wm;
+                const unsigned owner = __ballot_sync(0xffffffffu, cv == wm);
+                if (lane == __ffs(owner) - 1) cv = -INFINITY;   // one maximum leaves per round
             }
         }
         if (lane == 0) { s_red[warp] = make_float2(m, sum); s_rs[warp] = tw; }
@@ -191,45 +259,54 @@ beam_step_kernel(const uint16_t* __restrict__ logits, const float* __restrict__ 
         __syncthreads();
         float thr = -INFINITY;
         for (int q = 0; q < kWarps; ++q) thr = fmaxf(thr, s_rs[q]);
-        if (tid == 0) {
-            float M = -INFINITY, S = 0.f;
-            for (int q = 0; q < kWarps; ++q) {
-                const float nm = fmaxf(M, s_red[q].x);
-                S = (nm == -INFINITY) ? 0.f : S * exp2f(M - nm) + s_red[q].y * exp2f(s_red[q].x - nm);
+        if (warp == 0) {                           // the row's log-sum-exp, by shuffles
+            float M = lane < kWarps ? s_red[lane].x : -INFINITY;
+            float S = lane < kWarps ? s_red[lane].y : 0.f;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float om = __shfl_xor_sync(0xffffffffu, M, o);
+                const float os = __shfl_xor_sync(0xffffffffu, S, o);
+                const float nm = fmaxf(M, om);
+                S = (nm == -INFINITY) ? 0.f : S * ex2(M - nm) + os * ex2(om - nm);
                 M = nm;
             }
-            out.lse = (M + log2f(S)) * kLn2;
+            if (lane == 0) out.lse = (M + log2f(S)) * kLn2;
         }
-        // ---- pass 2: the tokens that reach the threshold (from L1/L2) -----------
-        for_row([&](float x, int v) {
-            if (x >= thr) {
+        // ---- pass 2: the tokens that reach the threshold -------------------------
+        auto keep = [&](float xv, int v) {
+            if (xv >= thr) {
                 const int k = atomicAdd(&s_cnt, 1);
-                if (k < kCap) { s_cv[k] = x; s_ci[k] = v; }
+                if (k < kCap) { s_cv[k] = xv; s_ci[k] = v; }
             }
-        });
+        };
+        if (in_regs) {
+#pragma unroll
+            for (int q = 0; q < kRegQ; ++q) {
+                const int i = tid + q * kThreads;
+                if (i < n4 && group_max(x[q]) >= thr) {   // most groups hold no candidate
+                    const uint32_t xw[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        keep(lo_bf16(xw[e]), i * 8 + 2 * e);
+                        keep(hi_bf16(xw[e]), i * 8 + 2 * e + 1);
+                    }
+                }
+            }
+        } else {
+            for_row(keep);                         // a second read, from L1/L2
+        }
         __syncthreads();
         const int cnt = s_cnt;
         if (cnt <= kCap) {
-            // the row's W best among the candidates, by one warp
-            if (warp == 0) {
-                for (int r = 0; r < W; ++r) {
-                    float ws = -INFINITY;
-                    int wi = kNoIndex, wk = -1;
-                    for (int q = lane; q < cnt; q += 32)
-                        if (s_ci[q] != kNoIndex && before(s_cv[q], s_ci[q], ws, wi)) {
-                            ws = s_cv[q]; wi = s_ci[q]; wk = q;
-                        }
-                    const int mine = wi;
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        const float os = __shfl_xor_sync(0xffffffffu, ws, o);
-                        const int oi = __shfl_xor_sync(0xffffffffu, wi, o);
-                        if (before(os, oi, ws, wi)) { ws = os; wi = oi; }
-                    }
-                    if (lane == 0) { out.val[r] = ws; out.tok[r] = wi; }
-                    if (mine != kNoIndex && mine == wi) s_ci[wk] = kNoIndex;   // taken
-                    __syncwarp();
-                }
+            // the row's W best among the candidates: a candidate's place is the
+            // number of candidates before it (tokens differ, so the order is strict)
+            if (tid < W && tid >= cnt) { out.val[tid] = -INFINITY; out.tok[tid] = kNoIndex; }
+            for (int c = tid; c < cnt; c += kThreads) {
+                const float cv = s_cv[c];
+                const int ci = s_ci[c];
+                int place = 0;
+                for (int d = 0; d < cnt; ++d) place += before(s_cv[d], s_ci[d], cv, ci) ? 1 : 0;
+                if (place < W) { out.val[place] = cv; out.tok[place] = ci; }
             }
         } else {
             // more candidates than room (ties or -inf rows): every thread's best W,
@@ -260,40 +337,63 @@ beam_step_kernel(const uint16_t* __restrict__ logits, const float* __restrict__ 
         }
         __syncthreads();
     }
-    cl.sync();                                   // every row published
-
-    // ---- rank 0: the request's W best candidates -------------------------------
-    if (rank == 0) {
-        float ls[W];
-        int li[W];
-#pragma unroll
-        for (int q = 0; q < W; ++q) { ls[q] = -INFINITY; li[q] = kNoIndex; }
-        if (tid < W * W) {                           // candidate (row w, its q-th best)
-            const int w = tid / W, q = tid % W;
-            const RowOut<W>* ro = cl.map_shared_rank(&s_row[w / C], w % C);
-            const float lse = ro->lse;
-            const int tok = ro->tok[q];
-            if (lse != -INFINITY && tok != kNoIndex) {
-                ls[0] = scores_in[(size_t)b * W + w] + (ro->val[q] - lse);
-                li[0] = w * V + tok;
-            }
-        }
-        select(ls, li);
-        for (int k = tid; k < W * (t + 1); k += kThreads) {
-            const int r = k / (t + 1), pos = k % (t + 1);
-            const int fi = s_wi[r];
-            const bool ok = fi != kNoIndex && s_win[r] != -INFINITY;
-            const int pw = ok ? fi / V : 0, tok = ok ? fi % V : -1;
-            beams_out[((size_t)b * W + r) * (t + 1) + pos] =
-                pos < t ? (ok ? beams_in[((size_t)b * W + pw) * t + pos] : -1) : tok;
-            if (pos == 0) {
-                scores_out[(size_t)b * W + r] = ok ? s_win[r] : -INFINITY;
-                parent[(size_t)b * W + r] = ok ? pw : -1;
-                if (!ok) rd_flag(dev_status, RD_DEV_BAD_LENGTH);
-            }
+    // ---- every row into rank 0's shared memory ---------------------------------
+    __syncthreads();                             // s_row complete
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every CTA has started
+    {
+        constexpr int kWords = (int)(sizeof(RowOut<W>) / 4);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(cl.map_shared_rank(&s_all[0], 0));
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(&s_row[0]);
+        for (int e = tid; e < rows * kWords; e += kThreads) {
+            const int w = rank + (e / kWords) * C;
+            if (w < W) dst[w * kWords + e % kWords] = src[e];
         }
     }
-    cl.sync();                                   // rank 0 is done reading its peers
+    cl.sync();                                   // rows published to rank 0
+    if (rank != 0) return;                       // no shared memory of a peer is read after this
+
+    // ---- rank 0: the request's W best candidates ---------------------------------
+    // candidate (row w, its q-th best) in slot w W + q; its place among the W x W
+    // is the number of candidates before it (equal pairs: the lower slot first)
+    for (int c = tid; c < W * W; c += kThreads) {
+        const int w = c / W, q = c % W;
+        const RowOut<W>& ro = s_all[w];
+        float cs = -INFINITY;
+        int ci = kNoIndex;
+        if (ro.lse != -INFINITY && ro.tok[q] != kNoIndex) {
+            cs = s_sc[w] + (ro.val[q] - ro.lse);
+            ci = w * V + ro.tok[q];
+        }
+        s_cv[c] = cs;
+        s_ci[c] = ci;
+    }
+    __syncthreads();
+    for (int c = tid; c < W * W; c += kThreads) {
+        const float cs = s_cv[c];
+        const int ci = s_ci[c];
+        int place = 0;
+        for (int d = 0; d < W * W; ++d) {
+            const float ds = s_cv[d];
+            const int di = s_ci[d];
+            place += (before(ds, di, cs, ci) || (ds == cs && di == ci && d < c)) ? 1 : 0;
+        }
+        if (place < W) { s_win[place] = cs; s_wi[place] = ci; }
+    }
+    __syncthreads();
+    for (int k = tid; k < W * (t + 1); k += kThreads) {
+        const int r = k / (t + 1), pos = k % (t + 1);
+        const int fi = s_wi[r];
+        const bool ok = fi != kNoIndex && s_win[r] != -INFINITY;
+        const int pw = ok ? fi / V : 0, tok = ok ? fi % V : -1;
+        beams_out[((size_t)b * W + r) * (t + 1) + pos] =
+            pos < t ? (ok ? (stage_prefix ? s_bin[pw * t + pos]
+                                          : beams_in[((size_t)b * W + pw) * t + pos]) : -1) : tok;
+        if (pos == 0) {
+            scores_out[(size_t)b * W + r] = ok ? s_win[r] : -INFINITY;
+            parent[(size_t)b * W + r] = ok ? pw : -1;
+            if (!ok) rd_flag(dev_status, RD_DEV_BAD_LENGTH);
+        }
+    }
 }
 
 }  // namespace
@@ -304,7 +404,8 @@ cudaError_t rd_launch_beam_step(const void* logits, const float* scores_in,
                                 int32_t* dev_status, cudaStream_t stream)
 {
     const uint16_t* lg = static_cast<const uint16_t*>(logits);
-    const int C = W < kMaxCluster ? W : kMaxCluster;
+    int C = W < kMaxCluster ? W : kMaxCluster;
+    if ((long)B * C > (long)kCtasPerSm * rd_device_sm_count()) C = W < 4 ? W : 4;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(B * C));
     cfg.blockDim = dim3(kThreads);
