@@ -275,8 +275,8 @@ beam_step_kernel(const uint16_t* __restrict__ logits, const float* __restrict__ 
         // ---- pass 2: the tokens that reach the threshold -------------------------
         auto keep = [&](float xv, int v) {
             if (xv >= thr) {
-                const int k = atomicAdd(&s_cnt, 1);
-                if (k < kCap) { s_cv[k] = xv; s_ci[k] = v; }
+                const int slot = atomicAdd(&s_cnt, 1);
+                if (slot < kCap) { s_cv[slot] = xv; s_ci[slot] = v; }
             }
         };
         if (in_regs) {
@@ -315,9 +315,9 @@ beam_step_kernel(const uint16_t* __restrict__ logits, const float* __restrict__ 
             int li[W];
 #pragma unroll
             for (int q = 0; q < W; ++q) { ls[q] = -INFINITY; li[q] = kNoIndex; }
-            for_row([&](float x, int v) {
-                if (!before(x, v, ls[W - 1], li[W - 1])) return;
-                float cs = x;
+            for_row([&](float xv, int v) {
+                if (!before(xv, v, ls[W - 1], li[W - 1])) return;
+                float cs = xv;
                 int ci = v;
 #pragma unroll
                 for (int q = 0; q < W; ++q) {    // insert into the sorted list
