@@ -412,7 +412,9 @@ def measure_next_rows(cfg, inp, step, dev, peak: float) -> dict:
     bi = inp["beams"][:, :, :cfg.L - 1].contiguous()
     bout = rd.rd_beam_search_step(lg, sc, bi, dev_status=st)
     us = _time_us(lambda: rd.rd_beam_search_step(lg, sc, bi, out=bout, dev_status=st))
-    rows["rd_beam_search_step"] = {"us": us, "gbs": lg.numel() * 2 / us / 1e3}
+    nb = lg.numel() * 2                        # the drafter logits, read once
+    rows["rd_beam_search_step"] = {"us": us, "gbs": nb / us / 1e3, "frac": nb / us / 1e3 / peak,
+                                   "algorithmic_bytes": float(nb)}
     torch.cuda.synchronize()
     if int(st.item()) != 0:
         raise SystemExit(f"device status {int(st.item())} in the next-row calls")
