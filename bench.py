@@ -666,9 +666,9 @@ def run_ours(args):
             "e2e": e2e,
             "next_rows": next_rows,
             # per step: pack, attention (+ the merge launch when the batch takes
-            # chunk ranges), greedy accept, unpack
+            # chunk ranges), greedy accept (argmax, then acceptance), unpack
             "gpu_launches": (1 + (2 if rd.rd_tree_attention_workspace_size(
-                cfg.B, cfg.P_max, cfg.Hq, cfg.Hkv, cfg.D, max_ctx, dev) > 0 else 1) + 1 + 1) * K,
+                cfg.B, cfg.P_max, cfg.Hq, cfg.Hkv, cfg.D, max_ctx, dev) > 0 else 1) + 2 + 1) * K,
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)

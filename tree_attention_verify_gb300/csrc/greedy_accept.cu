@@ -7,14 +7,16 @@
 // row, so deduplicated positions are read once and [B, W, L, V] logits are never
 // formed.
 //
-// One launch.  CTA (x = p*splits + s, y = b) scans vocab chunk s of row (b, p)
-// with 16-byte streaming loads, reduces (max value, lowest index) in the CTA and
-// folds it into a 64-bit key with atomicMax: high word = order-preserving bits
-// of the fp32 value, low word = ~index, so the maximum key is the maximum value
-// with the lowest index.  After its atomic each CTA takes a ticket on its
-// request; the CTA that takes the last ticket decodes the keys, resets them and
-// the ticket to zero, and runs the acceptance for that request.  No CTA ever
-// waits for another.
+// Two launches.  Argmax grid: CTA (x = p*splits + s, y = b) scans vocab chunk s
+// of row (b, p) with 16-byte streaming loads, reduces (max value, lowest index)
+// in the CTA, folds it into a 64-bit key with atomicMax (high word =
+// order-preserving bits of the fp32 value, low word = ~index, so the maximum key
+// is the maximum value with the lowest index) and exits: no fence, no ticket, so
+// a CTA holds its slot only while it streams.  Acceptance grid, one CTA per
+// request: a programmatic-dependent launch, scheduled while the argmax grid
+// runs, that waits until that grid has completed and its keys are visible,
+// then decodes and resets the keys and runs the acceptance.  No CTA spins on
+// another.
 #include <cuda_bf16.h>
 
 #include "rd_internal.cuh"
@@ -69,7 +71,7 @@ __device__ __forceinline__ void better(float& best, int& bidx, float v, int i)
     if (v > best || (v == best && i < bidx)) { best = v; bidx = i; }
 }
 
-// Acceptance of request b (the CTA that took its last ticket): decode and reset
+// Acceptance of request b (its CTA of the acceptance grid): decode and reset
 // the argmax keys, then walk every beam.  The request's beams and unpacker rows
 // are staged in shared memory with one coalesced load when they fit, so a beam's
 // walk costs no dependent global round trips.
@@ -81,7 +83,7 @@ __device__ __noinline__ void accept_request(int b, int P_max, int V, int Pb, boo
                                             int32_t* __restrict__ best_beam,
                                             int32_t* __restrict__ n_accepted,
                                             int32_t* __restrict__ out_tokens,
-                                            unsigned long long* keys, unsigned int* tickets,
+                                            unsigned long long* keys,
                                             int32_t* dev_status, int* s_g, int* s_acc,
                                             int* s_bb, int* s_up)
 {
@@ -136,28 +138,18 @@ __device__ __noinline__ void accept_request(int b, int P_max, int V, int Pb, boo
             if (last >= 0 && last < Pb) ot[a] = s_g[last];
             else rd_flag(dev_status, RD_DEV_BAD_INDEX);
         }
-        tickets[b] = 0u;
     }
 }
 
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads)
-argmax_accept_kernel(const uint16_t* __restrict__ logits, int P_max, int V, int splits,
-                     int chunk, const int32_t* __restrict__ beams,
-                     const int32_t* __restrict__ unpacker,
-                     const int32_t* __restrict__ packed_len, int W, int L,
-                     int32_t* __restrict__ argmax_out, int32_t* __restrict__ accept_len,
-                     int32_t* __restrict__ best_beam, int32_t* __restrict__ n_accepted,
-                     int32_t* __restrict__ out_tokens, unsigned long long* keys,
-                     unsigned int* tickets, int32_t* dev_status)
+argmax_kernel(const uint16_t* __restrict__ logits, int P_max, int V, int splits, int chunk,
+              const int32_t* __restrict__ packed_len, unsigned long long* keys)
 {
+    // the acceptance grid may launch now: it waits for this grid to complete
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ float s_best[kThreads / RD_WARP];
     __shared__ int s_idx[kThreads / RD_WARP];
-    __shared__ int s_last;
-    __shared__ int s_g[RD_MAX_PACKED];
-    __shared__ int s_acc[RD_MAX_BEAMS];
-    __shared__ int s_bb[kStage];
-    __shared__ int s_up[kStage];
 
     const int b = blockIdx.y;
     const int p = blockIdx.x / splits;
@@ -219,22 +211,35 @@ argmax_accept_kernel(const uint16_t* __restrict__ logits, int P_max, int V, int 
             if (bidx != kNoIndex) atomicMax(keys + (size_t)b * P_max + p, make_key(best, bidx));
         }
     }
-    // ticket on the request; the last CTA finishes the request
-    if (tid == 0) {
-        __threadfence();
-        const unsigned t = atomicAdd(tickets + b, 1u);
-        s_last = (t == (unsigned)(P_max * splits) - 1u);
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
+}
+
+// Acceptance of request b, once every argmax key of the launch before is final
+// (a programmatic-dependent launch: griddepcontrol.wait returns when that grid
+// has completed and its writes are visible).
+__global__ void __launch_bounds__(kThreads)
+accept_kernel(int P_max, int V, const int32_t* __restrict__ beams,
+              const int32_t* __restrict__ unpacker, const int32_t* __restrict__ packed_len,
+              int W, int L, int32_t* __restrict__ argmax_out, int32_t* __restrict__ accept_len,
+              int32_t* __restrict__ best_beam, int32_t* __restrict__ n_accepted,
+              int32_t* __restrict__ out_tokens, unsigned long long* keys, int32_t* dev_status)
+{
+    __shared__ int s_g[RD_MAX_PACKED];
+    __shared__ int s_acc[RD_MAX_BEAMS];
+    __shared__ int s_bb[kStage];
+    __shared__ int s_up[kStage];
+    const int b = blockIdx.x;
+    const int Pb = __ldg(packed_len + b);
+    const bool bad_len = Pb < 0 || Pb > P_max;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     accept_request(b, P_max, V, Pb, bad_len, beams, unpacker, W, L, argmax_out, accept_len,
-                   best_beam, n_accepted, out_tokens, keys, tickets, dev_status, s_g, s_acc,
+                   best_beam, n_accepted, out_tokens, keys, dev_status, s_g, s_acc,
                    s_bb, s_up);
 }
 
 }  // namespace
 
+// keys [B*P_max] (64-bit), then one reserved 32-bit word per request (part of
+// the size rd.h states; never written, so the workspace stays zero)
 size_t rd_accept_workspace_bytes(int B, int P_max)
 {
     return (size_t)B * P_max * sizeof(unsigned long long) + (size_t)B * sizeof(unsigned int);
@@ -267,17 +272,27 @@ cudaError_t rd_launch_greedy_accept(const void* logits, int B, int P_max, int V,
 {
     const rd_accept_plan plan = rd_accept_make_plan(B, P_max, V);
     auto* keys = static_cast<unsigned long long*>(workspace);
-    auto* tickets = reinterpret_cast<unsigned int*>(keys + (size_t)B * P_max);
     const bool vec = (V % 8 == 0) && (reinterpret_cast<uintptr_t>(logits) % 16 == 0);
     dim3 grid((unsigned)(P_max * plan.splits), (unsigned)B);
     const uint16_t* lg = static_cast<const uint16_t*>(logits);
     if (vec)
-        argmax_accept_kernel<true><<<grid, kThreads, 0, stream>>>(
-            lg, P_max, V, plan.splits, plan.chunk, beams, unpacker, packed_len, W, L, argmax,
-            accept_len, best_beam, n_accepted, out_tokens, keys, tickets, dev_status);
+        argmax_kernel<true><<<grid, kThreads, 0, stream>>>(lg, P_max, V, plan.splits, plan.chunk,
+                                                           packed_len, keys);
     else
-        argmax_accept_kernel<false><<<grid, kThreads, 0, stream>>>(
-            lg, P_max, V, plan.splits, plan.chunk, beams, unpacker, packed_len, W, L, argmax,
-            accept_len, best_beam, n_accepted, out_tokens, keys, tickets, dev_status);
-    return cudaGetLastError();
+        argmax_kernel<false><<<grid, kThreads, 0, stream>>>(lg, P_max, V, plan.splits, plan.chunk,
+                                                            packed_len, keys);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)B);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, accept_kernel, P_max, V, beams, unpacker, packed_len, W, L,
+                              argmax, accept_len, best_beam, n_accepted, out_tokens, keys,
+                              dev_status);
 }

@@ -2,7 +2,7 @@
 // allocate device memory.
 //
 // rd_greedy_accept needs a small scratch area (one 64-bit argmax key per packed
-// row and one ticket per request).  Its caller normally allocates it.  Some
+// row and one reserved word per request).  Its caller normally allocates it.  Some
 // callers cannot: code that runs inside a memory pool they do not own, plugins
 // whose host framework forbids cudaMalloc on the serving path, or runtimes that
 // must not allocate after start-up because an allocation can synchronise the
@@ -10,7 +10,7 @@
 // a fixed array in device global memory instead, owned by the library.
 //
 // Limits and sharing:
-//  - the array holds kMaxRows argmax keys and kMaxRequests tickets
+//  - the array holds kMaxRows argmax keys and kMaxRequests reserved words
 //    (B * P_max <= 65536 and B <= 65535, else RD_ERR_UNSUPPORTED);
 //    every GPU that loads librd holds it (about 768 KB) until the process exits;
 //  - every call on a device uses the same array: calls whose kernels overlap on
@@ -77,7 +77,7 @@ extern "C" rd_status rd_greedy_accept_noalloc(const void* logits, int B, int P_m
         return RD_ERR_INVALID_ARG;
     void* scratch = nullptr;
     if (scratch_ptr(&scratch) != cudaSuccess) return RD_ERR_CUDA;
-    // the kernel expects keys [B*P_max] (64-bit) followed by tickets [B] (32-bit), all zero
+    // the kernels expect keys [B*P_max] (64-bit) followed by B reserved 32-bit words, all zero
     cudaStream_t s = (cudaStream_t)stream;
     const size_t used = (size_t)B * P_max * sizeof(unsigned long long) + (size_t)B * sizeof(unsigned int);
     if (cudaMemsetAsync(scratch, 0, used, s) != cudaSuccess) return RD_ERR_CUDA;
