@@ -48,12 +48,13 @@ def _check(lg, s_in, beams_in, got):
 
 # rows of up to 32768 tokens are held in registers, longer ones streamed; a
 # batch of 40 requests at W = 8 takes clusters of four CTAs (two rows each),
-# smaller ones one row per CTA; t = 0 is the first step (no beam prefix yet)
+# smaller ones one row per CTA; t = 0 is the first step (no beam prefix yet);
+# 64 requests at W = 5 take clusters of four whose second rows mostly run past W
 @pytest.mark.parametrize("B,W,V,t,ties", [(16, 8, 32000, 3, False), (4, 5, 1000, 1, True),
                                           (2, 16, 128256, 4, False), (3, 1, 77, 2, False),
                                           (2, 8, 32768, 2, False), (2, 8, 32776, 2, False),
                                           (40, 8, 1000, 2, True), (3, 16, 32000, 1, False),
-                                          (3, 4, 1000, 0, False)])
+                                          (3, 4, 1000, 0, False), (64, 5, 1000, 1, False)])
 def test_beam_search_step(B, W, V, t, ties):
     import tree_attention_verify_gb300 as rd
     g = torch.Generator(device=DEV).manual_seed(W * V + t)
